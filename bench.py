@@ -1,0 +1,403 @@
+"""Benchmark: key-value LSD radix sort of 2^28 u32 keys with a u32 index
+payload, 8-bit digits (4 passes), on one GB300 (or N independent replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--n LOG2] [--no-distributions] [--no-e2e] [--no-cpu-baseline]
+
+Prints one JSON line on rank 0.  `value` is sorted keys per second with the
+inputs already in HBM (inputs of 2 GiB, larger than L2, so no flush is
+needed); `e2e` is the same sort through the C ABI with the keys and payloads
+copied from pinned host memory and the result copied back inside the timed
+region.  `roofline` reports the onesweep scatter kernel (the dominant one)
+against the measured HBM copy bandwidth; `cpu_baseline` times the CPU oracle
+on a bounded sample of the same workload.  Under torchrun each rank sorts its
+own replica (the sort has no exchange step); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Gkeys/s sorted (u32 keys & pairs, 2^28) + achieved HBM GB/s vs GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+DIGIT_BITS = 8
+KEY_BYTES = 4
+VAL_BYTES = 4
+
+
+def ideal_bytes(n: int, passes: int, key_bytes: int, val_bytes: int) -> int:
+    """One read of the keys for all histograms, then per pass one read and
+    one write of every key and payload."""
+    return n * key_bytes + passes * 2 * n * (key_bytes + val_bytes)
+
+
+def sweep_bytes_per_launch(n: int, key_bytes: int, val_bytes: int) -> int:
+    return 2 * n * (key_bytes + val_bytes)
+
+
+def workload_name(n_log2: int) -> str:
+    return (f"key-value sort, 2^{n_log2} u32 keys (uniform 32-bit, seed 0) + u32 index payload, "
+            f"{DIGIT_BITS}-bit digits ({32 // DIGIT_BITS} passes)")
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def onesweep_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("onesweep.cuh", "sweep_u32.cu", "kernels.h", "common.cuh", "keys.cuh"):
+        with open(os.path.join(ROOT, "lsd_radix_sort_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(n: int):
+    """DRAM bytes per onesweep launch from the committed ncu summary, scaled to
+    n keys, or None when the kernel source changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "onesweep_u32_pairs_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_hash") != onesweep_source_hash():
+        return None
+    return int(d["dram_bytes_per_key"] * n)
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (the job's time is its slowest replica)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_oracle_rate(n_sample: int, reps: int = 1):
+    """Time the CPU oracle (as it stands, one thread) on a sample of the workload."""
+    import oracle
+    from lsd_radix_sort_gb300 import workloads
+    keys = workloads.u32_uniform(n_sample, 0)
+    vals = workloads.index_payload(n_sample)
+    oracle.build()
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        oracle.sort(keys, vals, 0, 32, DIGIT_BITS)
+        times.append(time.perf_counter() - t0)
+    return n_sample / statistics.median(times) / 1e9, statistics.median(times)
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle on the host cores, bounded samples."""
+    if rank != 0:
+        return
+    n_sample = 1 << args.ref_log2
+    import oracle
+    from lsd_radix_sort_gb300 import workloads
+    oracle.build()
+    keys = workloads.u32_uniform(n_sample, 0)
+    vals = workloads.index_payload(n_sample)
+    for _ in range(args.warmup):
+        oracle.sort(keys, vals, 0, 32, DIGIT_BITS)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.sort(keys, vals, 0, 32, DIGIT_BITS)
+    dt = (time.perf_counter() - t0) / args.steps
+    v = n_sample / dt / 1e9
+    sample = f"2^{args.ref_log2} keys of the same uniform u32 key-value workload per step"
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "Gkeys/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+            "config": {"workload": workload_name(args.n_log2), "sample_keys": n_sample},
+            "cpu_baseline": {"value": v, "unit": "Gkeys/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "Gkeys/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def time_sorts(rs, torch, dk, dv, ko, vo, temp, steps, warmup, stream):
+    for _ in range(warmup):
+        rs.radix_sort_pairs(dk, dv, ko, vo, 0, 32, DIGIT_BITS, temp=temp)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        rs.radix_sort_pairs(dk, dv, ko, vo, 0, 32, DIGIT_BITS, temp=temp)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(stop) / steps
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--n", dest="n_log2", type=int, default=28)
+    ap.add_argument("--ref-log2", type=int, default=24)
+    ap.add_argument("--cpu-log2", type=int, default=26)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-distributions", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import lsd_radix_sort_gb300 as rs
+    from lsd_radix_sort_gb300 import build, workloads
+
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build.build()
+    rs.load_library()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    n = 1 << args.n_log2
+    passes = 32 // DIGIT_BITS
+
+    keys = workloads.u32_uniform(n, 0)
+    vals = workloads.index_payload(n)
+    dk = torch.from_numpy(keys.view(np.int32)).to(dev)
+    dv = torch.from_numpy(vals.view(np.int32)).to(dev)
+    ko = torch.empty_like(dk)
+    vo = torch.empty_like(dv)
+    temp = torch.empty(rs.temp_bytes(n, 4, 4, 0, 32, DIGIT_BITS), dtype=torch.uint8, device=dev)
+
+    # ---- device-resident timed region (with per-kernel events) ----------
+    for _ in range(args.warmup):
+        rs.radix_sort_pairs(dk, dv, ko, vo, 0, 32, DIGIT_BITS, temp=temp)
+    torch.cuda.synchronize()
+    rs.profile_read()
+    rs.launch_count_reset()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    rs.profile_enable(True)
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(args.steps):
+        rs.radix_sort_pairs(dk, dv, ko, vo, 0, 32, DIGIT_BITS, temp=temp)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    rs.profile_enable(False)
+    barrier(world)
+    clocks = sampler.stop()
+    launches = rs.launch_count_reset()
+    ms = start.elapsed_time(stop) / args.steps
+    recs = rs.profile_read()
+    status = rs.device_status(temp)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed sorts")
+    ms_max = max_over_ranks(ms, world, dev)
+    value = world * n / (ms_max * 1e-3) / 1e9
+
+    per_kernel = {}
+    for name, kms, units in recs:
+        d = per_kernel.setdefault(name, [0, 0.0])
+        d[0] += 1
+        d[1] += kms
+    sweep_launches, sweep_ms = per_kernel.get("onesweep", [0, 0.0])
+    sweep_avg = sweep_ms / max(sweep_launches, 1)
+    peak, peak_kind = load_peaks()
+    achieved = sweep_bytes_per_launch(n, KEY_BYTES, VAL_BYTES) / (sweep_avg * 1e-3) / 1e9
+    total_ideal = ideal_bytes(n, passes, KEY_BYTES, VAL_BYTES)
+    roofline = {"bound": "hbm", "kernel": "onesweep (one scatter pass)",
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
+                "traffic": recorded_traffic(n),
+                "algorithmic_bytes_per_launch": sweep_bytes_per_launch(n, KEY_BYTES, VAL_BYTES),
+                "avg_launch_ms": sweep_avg}
+    kernels = {k: {"launches": c, "total_ms": t, "share": t / max(sum(x[1] for x in
+                                                                      per_kernel.values()), 1e-9)}
+               for k, (c, t) in per_kernel.items()}
+
+    # ---- end to end through host buffers ---------------------------------
+    e2e = None
+    if not args.no_e2e:
+        hk = torch.from_numpy(keys.view(np.int32)).pin_memory()
+        hv = torch.from_numpy(vals.view(np.int32)).pin_memory()
+        hko = torch.empty_like(hk).pin_memory()
+        hvo = torch.empty_like(hv).pin_memory()
+        dk2, dv2 = torch.empty_like(dk), torch.empty_like(dv)
+
+        def e2e_step():
+            dk2.copy_(hk, non_blocking=True)
+            dv2.copy_(hv, non_blocking=True)
+            rs.radix_sort_pairs(dk2, dv2, ko, vo, 0, 32, DIGIT_BITS, temp=temp)
+            hko.copy_(ko, non_blocking=True)
+            hvo.copy_(vo, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        s1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = max_over_ranks(s0.elapsed_time(s1) / args.e2e_steps, world, dev)
+        e2e = {"value": world * n / (e_ms * 1e-3) / 1e9, "unit": "Gkeys/s",
+               "h2d_bytes_per_step": hk.numel() * 4 + hv.numel() * 4,
+               "d2h_bytes_per_step": hko.numel() * 4 + hvo.numel() * 4,
+               "ms_per_step": e_ms}
+        del hk, hv, hko, hvo, dk2, dv2
+
+    # ---- the other key distributions of the same workload ----------------
+    dists = None
+    if not args.no_distributions:
+        dists = {}
+        for name, gen in workloads.U32_DISTRIBUTIONS.items():
+            if name == "uniform":
+                dms = ms
+            else:
+                kk = gen(n, 0)
+                dk.copy_(torch.from_numpy(kk.view(np.int32)))
+                del kk
+                dms = time_sorts(rs, torch, dk, dv, ko, vo, temp, max(args.steps // 2, 3), 3,
+                                 stream)
+            dists[name] = {"ms": dms, "gkeys_s": n / (dms * 1e-3) / 1e9,
+                           "hbm_frac": total_ideal / (dms * 1e-3) / 1e9 / peak}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, secs = cpu_oracle_rate(1 << args.cpu_log2)
+        cpu = {"value": rate, "unit": "Gkeys/s", "cores": 1, "kind": "oracle",
+               "sample": f"2^{args.cpu_log2} keys of the same uniform u32 key-value workload, "
+                         f"one sort, {secs:.1f} s on one host thread"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "Gkeys/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "u32", "data": "synthetic",
+                "config": {"workload": workload_name(args.n_log2), "n_keys": n,
+                           "digit_bits": DIGIT_BITS, "passes": passes,
+                           "l2": "inputs larger than L2 (2 GiB keys+payload vs 129 MB L2), no flush",
+                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                "hbm": {"ideal_bytes_per_sort": total_ideal,
+                        "achieved_gbs": total_ideal / (ms_max * 1e-3) / 1e9,
+                        "frac_of_peak": total_ideal / (ms_max * 1e-3) / 1e9 / peak},
+                "e2e": e2e, "gpu_launches": launches, "kernels": kernels,
+                "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks,
+                "distributions": dists}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,197 @@
+/*
+ * lsdrs -- least-significant-digit radix sort for NVIDIA GB300 (sm_103a).
+ *
+ * The method (CUDA Handbook ch. 16 "Radix Sort", opening section and
+ * Listings 16-8/16-9; DSA CUDA from First Principles ch. 13, sections
+ * 13.1-13.3): keys are sorted one b-bit digit at a time, least significant
+ * digit first.  Each pass histograms the digit, turns the counts into bucket
+ * bases with an exclusive scan, and scatters every key stably to
+ * base[digit] + (number of earlier keys with the same digit).  Passes
+ * ping-pong between two buffers.
+ *
+ * On the GPU one sort is: an upfront kernel that reads the keys once and
+ * counts the digits of every pass; a scan kernel that turns those counts
+ * into bases; then one "onesweep" scatter kernel per pass, in which tiles
+ * rank their keys in shared memory, learn the counts of earlier tiles by a
+ * decoupled look-back, and write each digit's keys as one contiguous run.
+ *
+ * Conventions shared by every call:
+ *  - Pointers marked (device) are device memory of the current device; the
+ *    caller owns all of them, including `temp`.  The library allocates
+ *    nothing on the sort path.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Every sort call is asynchronous: it validates on the host,
+ *    enqueues its kernels on `stream` and returns; it never synchronises.
+ *  - Inputs are never written (sorting is out of place; "100 Days of GPU"
+ *    day 35, Pitfalls: never re-sort your own output).  keys_out may equal
+ *    keys_in (and vals_out vals_in) for an in-place sort; any other overlap
+ *    is rejected.
+ *  - Sorting is stable and ascending on bits [begin_bit, end_bit) of the
+ *    key; bits outside that range do not take part in the order but are
+ *    carried in the output keys.  The number of passes is
+ *    ceil((end_bit - begin_bit) / digit_bits); the last digit may be
+ *    narrower.
+ *  - Host-side argument errors return RS_ERR_INVALID or
+ *    RS_ERR_TEMP_TOO_SMALL before anything is enqueued.  A failed launch
+ *    returns RS_ERR_CUDA.  Errors raised on the device (a look-back wait
+ *    that exceeded its time limit) are recorded in `temp` and returned by
+ *    radix_sort_device_status().
+ */
+#ifndef LSDRS_H
+#define LSDRS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rs_status {
+  RS_OK = 0,
+  RS_ERR_INVALID = 1,          /* bad argument, found before any launch */
+  RS_ERR_TEMP_TOO_SMALL = 2,   /* temp_bytes below the size query's answer */
+  RS_ERR_CUDA = 3,             /* a CUDA runtime call or launch failed */
+  RS_ERR_LOOKBACK_TIMEOUT = 4  /* device: a look-back wait ran out of time */
+} rs_status;
+
+typedef enum rs_float_kind { RS_F16 = 0, RS_BF16 = 1 } rs_float_kind;
+
+/* Largest number of keys in one sort (or one row of a row-wise sort): the
+ * look-back words hold 30-bit counts. */
+#define RS_MAX_KEYS ((size_t)((1u << 30) - 1u))
+
+/* Size in bytes of the scratch buffer a flat sort needs.
+ *   n           number of keys (0 <= n <= RS_MAX_KEYS)
+ *   key_bytes   4 (u32) or 8 (u64)
+ *   value_bytes 0 (keys only) or 4 (u32 payload)
+ *   begin_bit, end_bit, digit_bits  as for the sort calls
+ * Writes the size to *bytes.  Host only; enqueues nothing. */
+rs_status radix_sort_temp_bytes(size_t n, int key_bytes, int value_bytes,
+                                int begin_bit, int end_bit, int digit_bits,
+                                size_t* bytes);
+
+/* Keys-only LSD radix sort of n unsigned 32-bit keys.
+ * (CUDA Handbook ch. 16, Listing 16-9 "RadixSort": one counting-sort pass per
+ * digit, ping-ponging between two buffers.)
+ *   keys_in   (device) n keys, read only
+ *   keys_out  (device) n keys, the sorted result
+ *   n         0 <= n <= RS_MAX_KEYS; n == 0 enqueues nothing
+ *   begin_bit 0 <= begin_bit < end_bit <= 32
+ *   digit_bits 1..8 (2^digit_bits buckets per pass)
+ *   temp, temp_bytes (device) scratch of at least radix_sort_temp_bytes()
+ *   stream    cudaStream_t as void* */
+rs_status radix_sort_keys_u32(const uint32_t* keys_in, uint32_t* keys_out, size_t n,
+                              int begin_bit, int end_bit, int digit_bits,
+                              void* temp, size_t temp_bytes, void* stream);
+
+/* As radix_sort_keys_u32 for unsigned 64-bit keys; end_bit <= 64. */
+rs_status radix_sort_keys_u64(const uint64_t* keys_in, uint64_t* keys_out, size_t n,
+                              int begin_bit, int end_bit, int digit_bits,
+                              void* temp, size_t temp_bytes, void* stream);
+
+/* Key-value sort: a u32 payload rides with every key move, so equal keys
+ * keep their payloads in input order ("100 Days of GPU", day 35, Exercise:
+ * carry a second array through the sort).
+ *   vals_in   (device) n payloads, read only
+ *   vals_out  (device) n payloads, permuted like the keys
+ * Other arguments as radix_sort_keys_u32. */
+rs_status radix_sort_pairs_u32(const uint32_t* keys_in, uint32_t* keys_out,
+                               const uint32_t* vals_in, uint32_t* vals_out, size_t n,
+                               int begin_bit, int end_bit, int digit_bits,
+                               void* temp, size_t temp_bytes, void* stream);
+
+/* As radix_sort_pairs_u32 with unsigned 64-bit keys. */
+rs_status radix_sort_pairs_u64(const uint64_t* keys_in, uint64_t* keys_out,
+                               const uint32_t* vals_in, uint32_t* vals_out, size_t n,
+                               int begin_bit, int end_bit, int digit_bits,
+                               void* temp, size_t temp_bytes, void* stream);
+
+/* Scratch size of a row-wise sort of a (rows, cols) 16-bit array. */
+rs_status radix_segmented_sort_temp_bytes(int64_t rows, int64_t cols, size_t* bytes);
+
+/* Row-wise stable sort of 16-bit floats along the last dimension, returning
+ * the sorted values and their int64 column indices (FlagTree PR #1084: a
+ * radix `sort` of fp16/bf16 rows with a descending flag folded into an
+ * order-preserving key, two 8-bit passes, int32 indices inside and int64 on
+ * the way out).
+ *   in        (device) rows*cols 16-bit patterns, row-major, contiguous
+ *   vals_out  (device) rows*cols patterns: each row sorted
+ *   idx_out   (device) rows*cols int64: idx_out[r][j] is the column of in[r]
+ *             that landed at position j
+ *   rows >= 0, 0 <= cols <= RS_MAX_KEYS; rows*cols == 0 enqueues nothing
+ *   kind      RS_F16 or RS_BF16 (both orders come from the sign bit, so the
+ *             result does not depend on it; it is validated and recorded)
+ *   descending 0 = ascending, 1 = descending.  Ascending order is the order
+ *             of the bijection T(u) = sign ? ~u : u | 0x8000: -NaN < -inf <
+ *             negatives < -0 < +0 < positives < +inf < +NaN; descending is
+ *             the order of ~T(u).  Equal patterns keep input order in both.
+ *   temp, temp_bytes (device) scratch of radix_segmented_sort_temp_bytes() */
+rs_status radix_segmented_sort_f16(const uint16_t* in, uint16_t* vals_out, int64_t* idx_out,
+                                   int64_t rows, int64_t cols, rs_float_kind kind,
+                                   int descending, void* temp, size_t temp_bytes,
+                                   void* stream);
+
+/* Upfront all-pass digit histograms and their exclusive scans, the first two
+ * stages of a sort, exposed on their own (FlagTree PR #1084, section 2:
+ * per-pass histograms of shape (passes, 2^b) from one read of the keys;
+ * DSA CUDA from First Principles section 13.1: bases are the exclusive
+ * prefix sums of the counts).
+ *   keys      (device) n keys of key_bytes (4 or 8) bytes
+ *   hist_out  (device) passes * 2^digit_bits u32 counts, pass-major
+ *   bases_out (device) the same shape: exclusive scan of each pass's counts
+ *   temp      (device) scratch of radix_sort_temp_bytes(n, key_bytes, 0, ...) */
+rs_status radix_sort_histograms(const void* keys, int key_bytes, size_t n,
+                                int begin_bit, int end_bit, int digit_bits,
+                                uint32_t* hist_out, uint32_t* bases_out,
+                                void* temp, size_t temp_bytes, void* stream);
+
+/* Synchronises `stream` and returns the device-side status of the last sort
+ * that used `temp` (RS_OK or RS_ERR_LOOKBACK_TIMEOUT), or RS_ERR_CUDA. */
+rs_status radix_sort_device_status(const void* temp, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* rs_status_string(rs_status status);
+
+/* Limit in nanoseconds on one look-back wait inside the scatter kernels
+ * (default 2 s).  A wait that runs past it records RS_ERR_LOOKBACK_TIMEOUT
+ * and releases every later tile.  Process-wide; host only. */
+rs_status rs_set_lookback_timeout_ns(uint64_t ns);
+
+/* Failure-detection check: runs the scatter kernels' bounded look-back wait
+ * on a status word that nothing ever sets, with the given limit
+ * (0 < timeout_ns <= 10 s).  Writes the status the wait produced
+ * (RS_ERR_LOOKBACK_TIMEOUT when it expired) to *result after synchronising
+ * `stream`.  word: (device) two u32 scratch words (the status word and an
+ * error word), overwritten. */
+rs_status rs_lookback_timeout_probe(uint32_t* word, uint64_t timeout_ns, void* stream,
+                                    rs_status* result);
+
+/* Bandwidth probe: copies `bytes` from src to dst with 16-byte vector loads
+ * and stores on every SM (the "copy, no sort" row of "100 Days of GPU",
+ * day 35, Results).  Both pointers (device), 16-byte aligned, bytes % 16 == 0. */
+rs_status rs_copy_probe(void* dst, const void* src, size_t bytes, void* stream);
+
+/* Per-kernel timing for measurement.  While enabled, every kernel the
+ * library enqueues is bracketed by two CUDA events on its stream.
+ * rs_profile_read synchronises on the last event and writes up to `max`
+ * records (kernel id, milliseconds, keys processed), oldest first, then
+ * clears the log; it returns the number written.  Kernel ids: 0 upfront
+ * histogram, 1 scan, 2 onesweep pass, 3 copy probe. */
+typedef struct rs_kernel_time {
+  int kernel;
+  float ms;
+  uint64_t units;
+} rs_kernel_time;
+rs_status rs_profile_enable(int enable);
+int rs_profile_read(rs_kernel_time* out, int max);
+
+/* Number of kernels the library enqueued since the last call (a launch
+ * count for measurement); resets the counter. */
+uint64_t rs_launch_count_reset(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LSDRS_H */

@@ -1,0 +1,454 @@
+// The C ABI (include/lsdrs.h): argument checks, the scratch layout, the pass
+// schedule and the launches.  Everything here runs on the host; each sort
+// enqueues K-HIST, K-SCAN and one K-SWEEP per pass on the caller's stream.
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace lsdrs;
+
+namespace {
+
+std::atomic<uint64_t> g_timeout_ns{2000000000ull};
+std::atomic<uint64_t> g_launches{0};
+
+// ---------------------------------------------------------------- profiling
+struct ProfRec {
+  int kernel;
+  uint64_t units;
+  cudaEvent_t start, stop;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof;
+
+// Runs `launch` bracketed by profiling events when enabled.
+template <class F>
+cudaError_t timed_launch(int kernel, uint64_t units, cudaStream_t s, F&& launch) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  ProfRec r{kernel, units, nullptr, nullptr};
+  bool prof;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    prof = g_prof_on;
+  }
+  if (prof) {
+    if (cudaEventCreate(&r.start) != cudaSuccess || cudaEventCreate(&r.stop) != cudaSuccess)
+      return cudaErrorUnknown;
+    cudaEventRecord(r.start, s);
+  }
+  cudaError_t e = launch();
+  if (prof) {
+    cudaEventRecord(r.stop, s);
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof.push_back(r);
+  }
+  return e;
+}
+
+// -------------------------------------------------------------------- plan
+// Scratch layout (offsets in bytes from `temp`, each 256-byte aligned):
+//   header   : word 0 = device error word, words 1..64 = tile counters
+//   status0  : look-back words of even passes  [tiles][radix] u32
+//   status1  : look-back words of odd passes   [tiles][radix] u32
+//   bases    : [rows][passes][radix] u32
+//   slots    : [rows][hist chunks][passes][radix] u32 partial histograms
+//   alt_keys : ping-pong key buffer
+//   alt_vals : ping-pong payload buffer (u32 / int32 indices)
+// header and status0 are contiguous: K-HIST zeroes them in one range.
+constexpr size_t kHeaderBytes = 512;
+constexpr int kMaxPasses = 64;
+
+struct Plan {
+  KeyKind key;
+  ValKind val;
+  int key_bytes;
+  int64_t rows, cols;
+  int begin_bit, end_bit, bits, passes, radix;
+  uint32_t last_mask;
+  int tile;
+  int64_t tiles_per_row, tiles;
+  int chunks_per_row;
+  int64_t chunk_len;
+  size_t off_status0, off_status1, off_bases, off_slots, off_alt_keys, off_alt_vals, total;
+};
+
+rs_status make_plan(KeyKind key, ValKind val, int64_t rows, int64_t cols, int begin_bit,
+                    int end_bit, int bits, Plan* out) {
+  Plan p{};
+  p.key = key;
+  p.val = val;
+  p.key_bytes = key == kKeyU32 ? 4 : key == kKeyU64 ? 8 : 2;
+  const int kbits = p.key_bytes * 8;
+  if (rows < 0 || cols < 0 || static_cast<uint64_t>(cols) > RS_MAX_KEYS) return RS_ERR_INVALID;
+  if (begin_bit < 0 || end_bit > kbits || begin_bit >= end_bit) return RS_ERR_INVALID;
+  if (bits < 1 || bits > 8) return RS_ERR_INVALID;
+  p.rows = rows;
+  p.cols = cols;
+  p.begin_bit = begin_bit;
+  p.end_bit = end_bit;
+  p.bits = bits;
+  p.passes = (end_bit - begin_bit + bits - 1) / bits;
+  if (p.passes > kMaxPasses) return RS_ERR_INVALID;
+  p.radix = 1 << bits;
+  const int last_w = end_bit - (begin_bit + (p.passes - 1) * bits);
+  p.last_mask = (1u << last_w) - 1u;
+  p.tile = sweep_shape(key, val).tile();
+  p.tiles_per_row = (cols + p.tile - 1) / p.tile;
+  p.tiles = rows * p.tiles_per_row;
+  // K-HIST chunking: enough CTAs to fill the GPU, at least kHistMinChunk keys each.
+  int64_t want = rows > 0 ? (kHistTargetCtas + rows - 1) / rows : 1;
+  int64_t max_chunks = (cols + kHistMinChunk - 1) / kHistMinChunk;
+  if (max_chunks < 1) max_chunks = 1;
+  if (want > max_chunks) want = max_chunks;
+  if (want < 1) want = 1;
+  p.chunks_per_row = static_cast<int>(want);
+  p.chunk_len = (cols + want - 1) / want;
+  p.chunk_len = static_cast<int64_t>(align_up(static_cast<size_t>(p.chunk_len), 64));
+
+  const size_t status_bytes = align_up(static_cast<size_t>(p.tiles) * p.radix * 4, 256);
+  const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols);
+  size_t off = kHeaderBytes;
+  p.off_status0 = off;
+  off += status_bytes;
+  p.off_status1 = off;
+  off += status_bytes;
+  p.off_bases = off;
+  off += align_up(static_cast<size_t>(rows) * p.passes * p.radix * 4, 256);
+  p.off_slots = off;
+  off += align_up(static_cast<size_t>(rows) * p.chunks_per_row * p.passes * p.radix * 4, 256);
+  p.off_alt_keys = off;
+  off += align_up(n * p.key_bytes, 256);
+  p.off_alt_vals = off;
+  if (val != kValNone) off += align_up(n * 4, 256);
+  p.total = off;
+  *out = p;
+  return RS_OK;
+}
+
+inline unsigned char* at(void* temp, size_t off) { return static_cast<unsigned char*>(temp) + off; }
+
+bool overlap(const void* a, size_t an, const void* b, size_t bn) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + bn && y < x + an;
+}
+
+// Enqueue K-HIST and K-SCAN.  hist_out: optional copy of the totals.
+rs_status run_front(const Plan& p, const void* keys, uint32_t flip, void* temp,
+                    uint32_t* hist_out, uint32_t* bases_out, cudaStream_t s) {
+  HistArgs h{};
+  h.keys = keys;
+  h.rows = p.rows;
+  h.cols = p.cols;
+  h.chunks_per_row = p.chunks_per_row;
+  h.chunk_len = p.chunk_len;
+  h.begin_bit = p.begin_bit;
+  h.passes = p.passes;
+  h.last_mask = p.last_mask;
+  h.flip = flip;
+  h.slots = reinterpret_cast<uint32_t*>(at(temp, p.off_slots));
+  h.zero_ptr = reinterpret_cast<uint32_t*>(temp);
+  h.zero_words = (p.off_status1) / 4;  // header + status0
+  const int64_t hgrid = p.rows * p.chunks_per_row;
+  const uint64_t n = static_cast<uint64_t>(p.rows) * p.cols;
+  cudaError_t e = timed_launch(0, n, s, [&] {
+    return launch_hist(p.key, p.bits, h, static_cast<int>(hgrid), s);
+  });
+  if (e != cudaSuccess) return RS_ERR_CUDA;
+  ScanArgs c{};
+  c.slots = h.slots;
+  c.rows = p.rows;
+  c.chunks_per_row = p.chunks_per_row;
+  c.passes = p.passes;
+  c.radix = p.radix;
+  c.hist_out = hist_out;
+  c.bases = bases_out ? bases_out : reinterpret_cast<uint32_t*>(at(temp, p.off_bases));
+  e = timed_launch(1, static_cast<uint64_t>(p.rows) * p.passes * p.radix, s,
+                   [&] { return launch_scan(c, s); });
+  return e == cudaSuccess ? RS_OK : RS_ERR_CUDA;
+}
+
+cudaError_t sweep(const Plan& p, const SweepArgs& a, cudaStream_t s) {
+  switch (p.key) {
+    case kKeyU32: return launch_sweep_u32(p.val, p.bits, a, p.tiles, s);
+    case kKeyU64: return launch_sweep_u64(p.val, p.bits, a, p.tiles, s);
+    case kKeyF16: return launch_sweep_f16(a, p.tiles, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// A whole sort: front stages, then one sweep per pass.  The pass that
+// writes `keys_out` last is chosen by parity so that no copy is needed,
+// except for an in-place sort with an odd number of passes.
+rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const void* vals_in,
+                   void* vals_out, uint32_t flip, void* temp, size_t temp_bytes,
+                   cudaStream_t s) {
+  const size_t n = static_cast<size_t>(p.rows) * static_cast<size_t>(p.cols);
+  if (n == 0) return RS_OK;
+  if (temp == nullptr) return RS_ERR_INVALID;
+  if (temp_bytes < p.total) return RS_ERR_TEMP_TOO_SMALL;
+  if (reinterpret_cast<uintptr_t>(temp) % 256 != 0) return RS_ERR_INVALID;
+  const size_t kb = static_cast<size_t>(p.key_bytes) * n;
+  const size_t vb_in = 4 * n;
+  const size_t vb_out = (p.val == kValIdx ? 8 : 4) * n;
+  if (!keys_in || !keys_out) return RS_ERR_INVALID;
+  if (p.val == kValU32 && (!vals_in || !vals_out)) return RS_ERR_INVALID;
+  if (p.val == kValIdx && !vals_out) return RS_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(keys_in) % p.key_bytes ||
+      reinterpret_cast<uintptr_t>(keys_out) % p.key_bytes)
+    return RS_ERR_INVALID;
+  if (keys_in != keys_out && overlap(keys_in, kb, keys_out, kb)) return RS_ERR_INVALID;
+  if (overlap(temp, p.total, keys_out, kb) || overlap(temp, p.total, keys_in, kb))
+    return RS_ERR_INVALID;
+  bool in_place = keys_in == keys_out;
+  if (p.val == kValU32) {
+    if (reinterpret_cast<uintptr_t>(vals_in) % 4 || reinterpret_cast<uintptr_t>(vals_out) % 4)
+      return RS_ERR_INVALID;
+    if (vals_in != vals_out && overlap(vals_in, vb_in, vals_out, vb_out)) return RS_ERR_INVALID;
+    if (overlap(keys_out, kb, vals_out, vb_out) || overlap(temp, p.total, vals_out, vb_out))
+      return RS_ERR_INVALID;
+    in_place = in_place || vals_in == vals_out;
+  }
+  if (p.val == kValIdx) {
+    if (reinterpret_cast<uintptr_t>(vals_out) % 8) return RS_ERR_INVALID;
+    if (overlap(keys_out, kb, vals_out, vb_out) || overlap(keys_in, kb, vals_out, vb_out) ||
+        overlap(temp, p.total, vals_out, vb_out))
+      return RS_ERR_INVALID;
+  }
+
+  rs_status st = run_front(p, keys_in, flip, temp, nullptr, nullptr, s);
+  if (st != RS_OK) return st;
+
+  uint32_t* header = reinterpret_cast<uint32_t*>(temp);
+  uint32_t* status[2] = {reinterpret_cast<uint32_t*>(at(temp, p.off_status0)),
+                         reinterpret_cast<uint32_t*>(at(temp, p.off_status1))};
+  void* alt_keys = at(temp, p.off_alt_keys);
+  void* alt_vals = at(temp, p.off_alt_vals);
+  const uint32_t* bases = reinterpret_cast<const uint32_t*>(at(temp, p.off_bases));
+  // kValIdx: the int32 indices live only in alt_vals; the last pass widens.
+  const bool odd_copy = in_place && (p.passes % 2 == 1) && p.val != kValIdx;
+  const void* ksrc = keys_in;
+  const void* vsrc = p.val == kValIdx ? nullptr : vals_in;
+  for (int q = 0; q < p.passes; ++q) {
+    const bool last = q == p.passes - 1;
+    bool to_out = odd_copy ? (q % 2 == 1) : ((p.passes - 1 - q) % 2 == 0);
+    SweepArgs a{};
+    a.keys_in = ksrc;
+    a.keys_out = to_out ? keys_out : alt_keys;
+    if (p.val == kValU32) {
+      a.vals_in = vsrc;
+      a.vals_out = to_out ? vals_out : alt_vals;
+    } else if (p.val == kValIdx) {
+      a.vals_in = vsrc;                       // null in the first pass: generate
+      a.vals_out = last ? vals_out : alt_vals;
+      a.wide_out = last ? 1 : 0;
+    }
+    a.rows = p.rows;
+    a.cols = p.cols;
+    a.tiles_per_row = p.tiles_per_row;
+    a.shift = p.begin_bit + q * p.bits;
+    a.mask = last ? p.last_mask : static_cast<uint32_t>(p.radix - 1);
+    a.flip = flip;
+    a.bases = bases + static_cast<size_t>(q) * p.radix;
+    a.bases_row_stride = static_cast<int64_t>(p.passes) * p.radix;
+    a.status = status[q & 1];
+    a.status_zero = last ? nullptr : status[(q + 1) & 1];
+    a.tile_counter = header + 1 + q;
+    a.error = header;
+    a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+    cudaError_t e = timed_launch(2, n, s, [&] { return sweep(p, a, s); });
+    if (e != cudaSuccess) return RS_ERR_CUDA;
+    ksrc = a.keys_out;
+    vsrc = a.vals_out;
+  }
+  if (odd_copy) {
+    if (cudaMemcpyAsync(keys_out, alt_keys, kb, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return RS_ERR_CUDA;
+    if (p.val == kValU32 &&
+        cudaMemcpyAsync(vals_out, alt_vals, vb_out, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+      return RS_ERR_CUDA;
+  }
+  return RS_OK;
+}
+
+rs_status flat_sort(KeyKind key, ValKind val, const void* ki, void* ko, const void* vi, void* vo,
+                    size_t n, int begin_bit, int end_bit, int bits, void* temp,
+                    size_t temp_bytes, void* stream) {
+  if (n > RS_MAX_KEYS) return RS_ERR_INVALID;
+  Plan p;
+  rs_status st = make_plan(key, val, 1, static_cast<int64_t>(n), begin_bit, end_bit, bits, &p);
+  if (st != RS_OK) return st;
+  return run_sort(p, ki, ko, vi, vo, 0u, temp, temp_bytes, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+rs_status radix_sort_temp_bytes(size_t n, int key_bytes, int value_bytes, int begin_bit,
+                                int end_bit, int digit_bits, size_t* bytes) {
+  if (!bytes || n > RS_MAX_KEYS) return RS_ERR_INVALID;
+  if (key_bytes != 4 && key_bytes != 8) return RS_ERR_INVALID;
+  if (value_bytes != 0 && value_bytes != 4) return RS_ERR_INVALID;
+  Plan p;
+  rs_status st = make_plan(key_bytes == 4 ? kKeyU32 : kKeyU64, value_bytes ? kValU32 : kValNone,
+                           1, static_cast<int64_t>(n), begin_bit, end_bit, digit_bits, &p);
+  if (st != RS_OK) return st;
+  *bytes = p.total;
+  return RS_OK;
+}
+
+rs_status radix_sort_keys_u32(const uint32_t* keys_in, uint32_t* keys_out, size_t n,
+                              int begin_bit, int end_bit, int digit_bits, void* temp,
+                              size_t temp_bytes, void* stream) {
+  return flat_sort(kKeyU32, kValNone, keys_in, keys_out, nullptr, nullptr, n, begin_bit, end_bit,
+                   digit_bits, temp, temp_bytes, stream);
+}
+
+rs_status radix_sort_keys_u64(const uint64_t* keys_in, uint64_t* keys_out, size_t n,
+                              int begin_bit, int end_bit, int digit_bits, void* temp,
+                              size_t temp_bytes, void* stream) {
+  return flat_sort(kKeyU64, kValNone, keys_in, keys_out, nullptr, nullptr, n, begin_bit, end_bit,
+                   digit_bits, temp, temp_bytes, stream);
+}
+
+rs_status radix_sort_pairs_u32(const uint32_t* keys_in, uint32_t* keys_out,
+                               const uint32_t* vals_in, uint32_t* vals_out, size_t n,
+                               int begin_bit, int end_bit, int digit_bits, void* temp,
+                               size_t temp_bytes, void* stream) {
+  return flat_sort(kKeyU32, kValU32, keys_in, keys_out, vals_in, vals_out, n, begin_bit, end_bit,
+                   digit_bits, temp, temp_bytes, stream);
+}
+
+rs_status radix_sort_pairs_u64(const uint64_t* keys_in, uint64_t* keys_out,
+                               const uint32_t* vals_in, uint32_t* vals_out, size_t n,
+                               int begin_bit, int end_bit, int digit_bits, void* temp,
+                               size_t temp_bytes, void* stream) {
+  return flat_sort(kKeyU64, kValU32, keys_in, keys_out, vals_in, vals_out, n, begin_bit, end_bit,
+                   digit_bits, temp, temp_bytes, stream);
+}
+
+rs_status radix_segmented_sort_temp_bytes(int64_t rows, int64_t cols, size_t* bytes) {
+  if (!bytes) return RS_ERR_INVALID;
+  Plan p;
+  rs_status st = make_plan(kKeyF16, kValIdx, rows, cols, 0, 16, 8, &p);
+  if (st != RS_OK) return st;
+  *bytes = p.total;
+  return RS_OK;
+}
+
+rs_status radix_segmented_sort_f16(const uint16_t* in, uint16_t* vals_out, int64_t* idx_out,
+                                   int64_t rows, int64_t cols, rs_float_kind kind,
+                                   int descending, void* temp, size_t temp_bytes,
+                                   void* stream) {
+  if (kind != RS_F16 && kind != RS_BF16) return RS_ERR_INVALID;
+  if (descending != 0 && descending != 1) return RS_ERR_INVALID;
+  Plan p;
+  rs_status st = make_plan(kKeyF16, kValIdx, rows, cols, 0, 16, 8, &p);
+  if (st != RS_OK) return st;
+  return run_sort(p, in, vals_out, nullptr, idx_out, descending ? 0xFFFFu : 0u, temp, temp_bytes,
+                  static_cast<cudaStream_t>(stream));
+}
+
+rs_status radix_sort_histograms(const void* keys, int key_bytes, size_t n, int begin_bit,
+                                int end_bit, int digit_bits, uint32_t* hist_out,
+                                uint32_t* bases_out, void* temp, size_t temp_bytes,
+                                void* stream) {
+  if (key_bytes != 4 && key_bytes != 8) return RS_ERR_INVALID;
+  if (n > RS_MAX_KEYS) return RS_ERR_INVALID;
+  Plan p;
+  rs_status st = make_plan(key_bytes == 4 ? kKeyU32 : kKeyU64, kValNone, 1,
+                           static_cast<int64_t>(n), begin_bit, end_bit, digit_bits, &p);
+  if (st != RS_OK) return st;
+  if (!hist_out || !bases_out || !temp) return RS_ERR_INVALID;
+  if (n > 0 && !keys) return RS_ERR_INVALID;
+  if (temp_bytes < p.total) return RS_ERR_TEMP_TOO_SMALL;
+  if (reinterpret_cast<uintptr_t>(temp) % 256 != 0) return RS_ERR_INVALID;
+  return run_front(p, keys, 0u, temp, hist_out, bases_out, static_cast<cudaStream_t>(stream));
+}
+
+rs_status radix_sort_device_status(const void* temp, void* stream) {
+  if (!temp) return RS_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, temp, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return RS_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RS_ERR_CUDA;
+  return word == kErrNone ? RS_OK : static_cast<rs_status>(word);
+}
+
+const char* rs_status_string(rs_status status) {
+  switch (status) {
+    case RS_OK: return "RS_OK";
+    case RS_ERR_INVALID: return "RS_ERR_INVALID";
+    case RS_ERR_TEMP_TOO_SMALL: return "RS_ERR_TEMP_TOO_SMALL";
+    case RS_ERR_CUDA: return "RS_ERR_CUDA";
+    case RS_ERR_LOOKBACK_TIMEOUT: return "RS_ERR_LOOKBACK_TIMEOUT";
+  }
+  return "RS_UNKNOWN";
+}
+
+rs_status rs_set_lookback_timeout_ns(uint64_t ns) {
+  if (ns == 0) return RS_ERR_INVALID;
+  g_timeout_ns.store(ns, std::memory_order_relaxed);
+  return RS_OK;
+}
+
+rs_status rs_lookback_timeout_probe(uint32_t* word, uint64_t timeout_ns, void* stream,
+                                    rs_status* result) {
+  if (!word || !result || timeout_ns == 0 || timeout_ns > 10000000000ull) return RS_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(word, 0, 8, s) != cudaSuccess) return RS_ERR_CUDA;
+  cudaError_t e = timed_launch(4, 1, s, [&] {
+    return launch_timeout_probe(word, word + 1, timeout_ns, s);
+  });
+  if (e != cudaSuccess) return RS_ERR_CUDA;
+  uint32_t err = 0;
+  if (cudaMemcpyAsync(&err, word + 1, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return RS_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RS_ERR_CUDA;
+  *result = err == kErrNone ? RS_OK : static_cast<rs_status>(err);
+  return RS_OK;
+}
+
+rs_status rs_copy_probe(void* dst, const void* src, size_t bytes, void* stream) {
+  if (!dst || !src || bytes % 16 != 0) return RS_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(dst) % 16 || reinterpret_cast<uintptr_t>(src) % 16)
+    return RS_ERR_INVALID;
+  if (bytes == 0) return RS_OK;
+  if (overlap(dst, bytes, src, bytes)) return RS_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = timed_launch(3, bytes, s, [&] { return launch_copy(dst, src, bytes, s); });
+  return e == cudaSuccess ? RS_OK : RS_ERR_CUDA;
+}
+
+rs_status rs_profile_enable(int enable) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = enable != 0;
+  return RS_OK;
+}
+
+int rs_profile_read(rs_kernel_time* out, int max) {
+  std::vector<ProfRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    recs.swap(g_prof);
+  }
+  int w = 0;
+  for (ProfRec& r : recs) {
+    float ms = -1.0f;
+    if (cudaEventSynchronize(r.stop) == cudaSuccess) cudaEventElapsedTime(&ms, r.start, r.stop);
+    if (out && w < max) out[w++] = rs_kernel_time{r.kernel, ms, r.units};
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  return w;
+}
+
+uint64_t rs_launch_count_reset(void) { return g_launches.exchange(0); }
+
+}  // extern "C"

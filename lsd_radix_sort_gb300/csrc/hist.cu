@@ -1,0 +1,266 @@
+// K-HIST: digit histograms of every pass from one read of the keys.
+// K-SCAN: per-pass exclusive scans of those counts into bucket bases.
+//
+// A pass only reorders keys, so the count of each digit of pass p is the
+// same in the unsorted input as in pass p's input; one read of the keys
+// therefore yields the histograms of all passes (FlagTree PR #1084,
+// section 2: "compute_global_hist_kernel" fills a (passes, 2^b) table per
+// row in one sweep).  Counting uses shared-memory counters private to the
+// CTA ("privatized" histograms, CUDA Handbook ch. 16 section 16.3, named in
+// the Radix Sort section as usable without modification), replicated over
+// kCols lane columns so that equal digits in one warp hit at most
+// 32 / kCols copies, plus run-length merging of equal consecutive digits per
+// thread so that skewed and constant inputs do not serialise on one counter.
+// Each CTA writes its partial counts to its own slot; K-SCAN adds the slots
+// and scans (DSA CUDA from First Principles, section 13.1: the base of digit
+// d is the exclusive prefix sum of the counts of the digits below it).
+#include "common.cuh"
+#include "kernels.h"
+#include "keys.cuh"
+
+namespace lsdrs {
+
+namespace {
+
+constexpr int kCols = 8;
+
+template <class KeyOp, int BITS>
+struct HistCfg {
+  static constexpr int kRadix = 1 << BITS;
+  static constexpr int kMaxPasses = (KeyOp::kBits + BITS - 1) / BITS;
+  static constexpr bool kMerge = kMaxPasses <= 8;
+  static constexpr int kVec = 16 / sizeof(typename KeyOp::T);
+  static constexpr int kUnroll = 4;
+  static size_t smem_bytes(int passes) {
+    return static_cast<size_t>(passes) * kRadix * kCols * sizeof(uint32_t);
+  }
+};
+
+template <class KeyOp, int BITS>
+struct Counter {
+  using Cfg = HistCfg<KeyOp, BITS>;
+  static constexpr int R = Cfg::kRadix;
+  static constexpr int MP = Cfg::kMerge ? Cfg::kMaxPasses : 1;
+  uint32_t* cnt;
+  uint32_t col;
+  int begin_bit, passes;
+  uint32_t last_mask, flip;
+  uint32_t cur_d[MP];
+  uint32_t cur_c[MP];
+
+  __device__ __forceinline__ void init() {
+#pragma unroll
+    for (int p = 0; p < MP; ++p) {
+      cur_d[p] = 0;
+      cur_c[p] = 0;
+    }
+  }
+  __device__ __forceinline__ uint32_t mask_of(int p) const {
+    return p == passes - 1 ? last_mask : static_cast<uint32_t>(R - 1);
+  }
+  __device__ __forceinline__ void add(typename KeyOp::T k) {
+    if constexpr (Cfg::kMerge) {
+#pragma unroll
+      for (int p = 0; p < MP; ++p) {
+        if (p < passes) {
+          uint32_t d = KeyOp::digit(k, begin_bit + p * BITS, mask_of(p), flip);
+          if (d == cur_d[p]) {
+            cur_c[p] += 1;
+          } else {
+            if (cur_c[p]) atomicAdd(&cnt[(p * R + cur_d[p]) * kCols + col], cur_c[p]);
+            cur_d[p] = d;
+            cur_c[p] = 1;
+          }
+        }
+      }
+    } else {
+      for (int p = 0; p < passes; ++p) {
+        uint32_t d = KeyOp::digit(k, begin_bit + p * BITS, mask_of(p), flip);
+        atomicAdd(&cnt[(p * R + d) * kCols + col], 1u);
+      }
+    }
+  }
+  __device__ __forceinline__ void flush() {
+    if constexpr (Cfg::kMerge) {
+#pragma unroll
+      for (int p = 0; p < MP; ++p)
+        if (p < passes && cur_c[p]) atomicAdd(&cnt[(p * R + cur_d[p]) * kCols + col], cur_c[p]);
+    }
+  }
+};
+
+template <class KeyOp, int BITS>
+__global__ void __launch_bounds__(kHistThreads) upfront_hist_kernel(HistArgs a) {
+  using T = typename KeyOp::T;
+  using Cfg = HistCfg<KeyOp, BITS>;
+  constexpr int R = Cfg::kRadix;
+  constexpr int V = Cfg::kVec;
+  constexpr int U = Cfg::kUnroll;
+  extern __shared__ __align__(16) uint32_t cnt[];
+
+  const int tid = threadIdx.x;
+  const int nb = a.passes * R;
+  for (int i = tid; i < nb * kCols; i += kHistThreads) cnt[i] = 0;
+
+  // Zero the look-back words and counters the sweeps start from.
+  {
+    const size_t stride = static_cast<size_t>(gridDim.x) * kHistThreads;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * kHistThreads + tid; i < a.zero_words;
+         i += stride)
+      a.zero_ptr[i] = 0;
+  }
+  __syncthreads();
+
+  const int64_t row = blockIdx.x / a.chunks_per_row;
+  const int chunk = blockIdx.x % a.chunks_per_row;
+  const int64_t begin = static_cast<int64_t>(chunk) * a.chunk_len;
+  const int64_t end = begin + a.chunk_len < a.cols ? begin + a.chunk_len : a.cols;
+  const T* base = static_cast<const T*>(a.keys) + row * a.cols;
+
+  Counter<KeyOp, BITS> c;
+  c.cnt = cnt;
+  c.col = tid & (kCols - 1);
+  c.begin_bit = a.begin_bit;
+  c.passes = a.passes;
+  c.last_mask = a.last_mask;
+  c.flip = a.flip;
+  c.init();
+
+  if (begin < end) {
+    // Split [begin, end) into a scalar head up to 16-byte alignment, a
+    // vectorised body and a scalar tail.
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(base + begin);
+    int64_t head = static_cast<int64_t>(((16 - (addr & 15)) & 15) / sizeof(T));
+    if (head > end - begin) head = end - begin;
+    const int64_t body_begin = begin + head;
+    const int64_t nvec = (end - body_begin) / V;
+    const int64_t body_end = body_begin + nvec * V;
+    if (tid < head) c.add(base[begin + tid]);
+    if (tid < end - body_end) c.add(base[body_end + tid]);
+
+    using Vec = uint4;
+    const Vec* vp = reinterpret_cast<const Vec*>(base + body_begin);
+    int64_t v = tid;
+    for (; v + (U - 1) * kHistThreads < nvec; v += U * kHistThreads) {
+      Vec buf[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) buf[u] = __ldcs(vp + v + u * kHistThreads);
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const T* ks = reinterpret_cast<const T*>(&buf[u]);
+#pragma unroll
+        for (int e = 0; e < V; ++e) c.add(ks[e]);
+      }
+    }
+    for (; v < nvec; v += kHistThreads) {
+      Vec b = __ldcs(vp + v);
+      const T* ks = reinterpret_cast<const T*>(&b);
+#pragma unroll
+      for (int e = 0; e < V; ++e) c.add(ks[e]);
+    }
+  }
+  c.flush();
+  __syncthreads();
+
+  uint32_t* slot = a.slots + (row * a.chunks_per_row + chunk) * static_cast<int64_t>(nb);
+  for (int b = tid; b < nb; b += kHistThreads) {
+    uint32_t s = 0;
+#pragma unroll
+    for (int k = 0; k < kCols; ++k) s += cnt[b * kCols + k];
+    slot[b] = s;
+  }
+}
+
+// One CTA per (row, pass): add the slots of the row's chunks, then an
+// exclusive scan over the digits.
+__global__ void __launch_bounds__(kScanThreads) digit_scan_kernel(ScanArgs a) {
+  __shared__ uint32_t warp_sums[kScanThreads / kWarp];
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int64_t row = blockIdx.x / a.passes;
+  const int p = blockIdx.x % a.passes;
+  const int nb = a.passes * a.radix;
+
+  uint32_t total = 0;
+  if (tid < a.radix) {
+    const uint32_t* s = a.slots + row * a.chunks_per_row * static_cast<int64_t>(nb) +
+                        p * a.radix + tid;
+    for (int c = 0; c < a.chunks_per_row; ++c) total += s[static_cast<int64_t>(c) * nb];
+  }
+  // block-wide exclusive scan of `total` over tid
+  uint32_t incl = total;
+#pragma unroll
+  for (int o = 1; o < kWarp; o <<= 1) {
+    uint32_t y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == kWarp - 1) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t w = lane < kScanThreads / kWarp ? warp_sums[lane] : 0;
+    uint32_t wi = w;
+#pragma unroll
+    for (int o = 1; o < kWarp; o <<= 1) {
+      uint32_t y = __shfl_up_sync(kFull, wi, o);
+      if (lane >= o) wi += y;
+    }
+    if (lane < kScanThreads / kWarp) warp_sums[lane] = wi - w;
+  }
+  __syncthreads();
+  const uint32_t excl = incl - total + warp_sums[warp];
+  if (tid < a.radix) {
+    const int64_t o = (row * a.passes + p) * a.radix + tid;
+    a.bases[o] = excl;
+    if (a.hist_out) a.hist_out[o] = total;
+  }
+}
+
+template <class KeyOp, int BITS>
+cudaError_t launch_hist_t(const HistArgs& a, int grid, cudaStream_t s) {
+  using Cfg = HistCfg<KeyOp, BITS>;
+  const size_t smem = Cfg::smem_bytes(a.passes);
+  auto kern = upfront_hist_kernel<KeyOp, BITS>;
+  if (smem > 48 * 1024) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<grid, kHistThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <class KeyOp>
+cudaError_t launch_hist_k(int bits, const HistArgs& a, int grid, cudaStream_t s) {
+  switch (bits) {
+    case 1: return launch_hist_t<KeyOp, 1>(a, grid, s);
+    case 2: return launch_hist_t<KeyOp, 2>(a, grid, s);
+    case 3: return launch_hist_t<KeyOp, 3>(a, grid, s);
+    case 4: return launch_hist_t<KeyOp, 4>(a, grid, s);
+    case 5: return launch_hist_t<KeyOp, 5>(a, grid, s);
+    case 6: return launch_hist_t<KeyOp, 6>(a, grid, s);
+    case 7: return launch_hist_t<KeyOp, 7>(a, grid, s);
+    case 8: return launch_hist_t<KeyOp, 8>(a, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_hist(KeyKind k, int bits, const HistArgs& a, int grid, cudaStream_t s) {
+  switch (k) {
+    case kKeyU32: return launch_hist_k<KeyU32>(bits, a, grid, s);
+    case kKeyU64: return launch_hist_k<KeyU64>(bits, a, grid, s);
+    case kKeyF16:
+      if (bits != 8) return cudaErrorInvalidValue;
+      return launch_hist_t<KeyF16Bits, 8>(a, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s) {
+  const int64_t grid = a.rows * a.passes;
+  digit_scan_kernel<<<static_cast<unsigned>(grid), kScanThreads, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace lsdrs

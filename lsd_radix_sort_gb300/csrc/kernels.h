@@ -1,0 +1,94 @@
+// Launch interface between the C ABI (api.cu) and the kernel translation
+// units.  Host-side structs only; no templates cross this boundary.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace lsdrs {
+
+enum KeyKind { kKeyU32 = 0, kKeyU64 = 1, kKeyF16 = 2 };
+// Payload carried with the keys: none, a u32 array, or a column index that
+// is generated in the first pass, kept as int32 and widened to int64 by the
+// last pass.
+enum ValKind { kValNone = 0, kValU32 = 1, kValIdx = 2 };
+
+// Threads per CTA and keys per thread of the onesweep kernel, per
+// (key, payload) combination.  The tile is THREADS * ITEMS keys.
+struct SweepShape {
+  int threads;
+  int items;
+  constexpr int tile() const { return threads * items; }
+};
+constexpr SweepShape kShapeU32Keys{512, 16};
+constexpr SweepShape kShapeU32Pairs{512, 12};
+constexpr SweepShape kShapeU64Keys{512, 8};
+constexpr SweepShape kShapeU64Pairs{512, 8};
+constexpr SweepShape kShapeF16Idx{512, 8};
+constexpr int kSweepMinBlocks = 2;
+constexpr SweepShape sweep_shape(KeyKind k, ValKind v) {
+  return k == kKeyU32 ? (v == kValNone ? kShapeU32Keys : kShapeU32Pairs)
+       : k == kKeyU64 ? (v == kValNone ? kShapeU64Keys : kShapeU64Pairs)
+                      : kShapeF16Idx;
+}
+
+constexpr int kHistThreads = 512;
+constexpr int kHistTargetCtas = 608;   // 152 SMs x 4 resident CTAs
+constexpr int64_t kHistMinChunk = 4096;
+constexpr int kScanThreads = 256;
+
+struct HistArgs {
+  const void* keys;
+  int64_t rows, cols;
+  int chunks_per_row;
+  int64_t chunk_len;
+  int begin_bit, passes;
+  uint32_t last_mask;      // digit mask of the last (possibly narrower) pass
+  uint32_t flip;           // 0xFFFF: descending 16-bit float keys
+  uint32_t* slots;         // [rows][chunks_per_row][passes][radix] counts
+  uint32_t* zero_ptr;      // words zeroed by the grid before any sweep
+  size_t zero_words;
+};
+
+struct ScanArgs {
+  const uint32_t* slots;
+  int64_t rows;
+  int chunks_per_row;
+  int passes;
+  int radix;
+  uint32_t* hist_out;      // optional [rows][passes][radix] totals
+  uint32_t* bases;         // [rows][passes][radix] exclusive scans
+};
+
+struct SweepArgs {
+  const void* keys_in;
+  void* keys_out;
+  const void* vals_in;     // null with kValIdx: generate column indices
+  void* vals_out;
+  int64_t rows, cols;
+  int64_t tiles_per_row;
+  int shift;
+  uint32_t mask;
+  uint32_t flip;
+  int wide_out;            // kValIdx: write int64 indices
+  const uint32_t* bases;   // bases of this pass for row 0
+  int64_t bases_row_stride;
+  uint32_t* status;        // [rows * tiles_per_row][radix] look-back words
+  uint32_t* status_zero;   // next pass's look-back words, zeroed here
+  uint32_t* tile_counter;
+  uint32_t* error;
+  uint64_t timeout_ns;
+};
+
+cudaError_t launch_hist(KeyKind k, int bits, const HistArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
+cudaError_t launch_sweep_u32(ValKind v, int bits, const SweepArgs& a, int64_t grid,
+                             cudaStream_t s);
+cudaError_t launch_sweep_u64(ValKind v, int bits, const SweepArgs& a, int64_t grid,
+                             cudaStream_t s);
+cudaError_t launch_sweep_f16(const SweepArgs& a, int64_t grid, cudaStream_t s);
+cudaError_t launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t s);
+cudaError_t launch_timeout_probe(uint32_t* word, uint32_t* error, uint64_t timeout_ns,
+                                 cudaStream_t s);
+
+}  // namespace lsdrs

@@ -1,0 +1,12 @@
+// Onesweep instantiation for 16-bit float rows: 8-bit digits of the
+// order-preserving key, column-index payload.
+#include "onesweep.cuh"
+
+namespace lsdrs {
+
+cudaError_t launch_sweep_f16(const SweepArgs& a, int64_t grid, cudaStream_t s) {
+  return launch_sweep_t<KeyF16Bits, 8, kValIdx, kShapeF16Idx.threads, kShapeF16Idx.items,
+                        kSweepMinBlocks>(a, grid, s);
+}
+
+}  // namespace lsdrs

@@ -1,0 +1,17 @@
+// Onesweep instantiations for unsigned 32-bit keys (keys only, u32 pairs).
+#include "onesweep.cuh"
+
+namespace lsdrs {
+
+cudaError_t launch_sweep_u32(ValKind v, int bits, const SweepArgs& a, int64_t grid,
+                             cudaStream_t s) {
+  if (v == kValNone)
+    return launch_sweep_bits<KeyU32, kValNone, kShapeU32Keys.threads, kShapeU32Keys.items,
+                             kSweepMinBlocks>(bits, a, grid, s);
+  if (v == kValU32)
+    return launch_sweep_bits<KeyU32, kValU32, kShapeU32Pairs.threads, kShapeU32Pairs.items,
+                             kSweepMinBlocks>(bits, a, grid, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace lsdrs

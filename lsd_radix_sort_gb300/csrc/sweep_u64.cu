@@ -1,0 +1,17 @@
+// Onesweep instantiations for unsigned 64-bit keys (keys only, u32 pairs).
+#include "onesweep.cuh"
+
+namespace lsdrs {
+
+cudaError_t launch_sweep_u64(ValKind v, int bits, const SweepArgs& a, int64_t grid,
+                             cudaStream_t s) {
+  if (v == kValNone)
+    return launch_sweep_bits<KeyU64, kValNone, kShapeU64Keys.threads, kShapeU64Keys.items,
+                             kSweepMinBlocks>(bits, a, grid, s);
+  if (v == kValU32)
+    return launch_sweep_bits<KeyU64, kValU32, kShapeU64Pairs.threads, kShapeU64Pairs.items,
+                             kSweepMinBlocks>(bits, a, grid, s);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace lsdrs

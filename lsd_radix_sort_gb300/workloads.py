@@ -188,23 +188,12 @@ def double_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return out
 
 
-def rows16(rows: int, cols: int, kind: str = "f16", seed: int = 0,
-           specials: bool = True) -> np.ndarray:
-    """(rows, cols) uint16 bit patterns of fp16 ("f16") or bf16 ("bf16") values.
-
-    Base value: standard normal by Box-Muller from two 53-bit uniforms
-    (streams 0 and 1), rounded to the format nearest-even.  With ``specials``:
-    for u = w(seed, 2, i) * 2**-64, [0,.01) +0, [.01,.02) -0, [.02,.03) +inf,
-    [.03,.04) -inf, [.04,.05) NaN (sign = bit 0 of w(seed, 3, i)) and
-    [.05,.15) a copy of the base value at column w(seed, 4, i) mod cols of the
-    same row.  i is the flat row-major index.
-    """
-    if kind not in ("f16", "bf16"):
-        raise ValueError("kind must be 'f16' or 'bf16'")
-    n = rows * cols
+def _rows16_block(out: np.ndarray, r0: int, rows: int, cols: int, kind: str, seed: int,
+                  specials: bool) -> None:
+    start, n = r0 * cols, rows * cols
     sh = np.uint64(11)
-    u1 = ((words(seed, 0, n) >> sh).astype(np.float64) + 1.0) * (2.0 ** -53)
-    u2 = (words(seed, 1, n) >> sh).astype(np.float64) * (2.0 ** -53)
+    u1 = ((words(seed, 0, n, start, 1) >> sh).astype(np.float64) + 1.0) * (2.0 ** -53)
+    u2 = (words(seed, 1, n, start, 1) >> sh).astype(np.float64) * (2.0 ** -53)
     z = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * np.pi * u2)
     del u1, u2
     if kind == "f16":
@@ -216,19 +205,48 @@ def rows16(rows: int, cols: int, kind: str = "f16", seed: int = 0,
     del z
     base = base.reshape(rows, cols)
     if not specials:
-        return np.ascontiguousarray(base)
-    out = base.copy()
-    u = (words(seed, 2, n) >> sh).astype(np.float64).reshape(rows, cols) * (2.0 ** -53)
-    nan_sign = (words(seed, 3, n) & np.uint64(1)).reshape(rows, cols).astype(bool)
-    src_col = (words(seed, 4, n) % np.uint64(cols)).astype(np.int64).reshape(rows, cols)
-    out[u < 0.01] = F16_PZERO
-    out[(u >= 0.01) & (u < 0.02)] = F16_NZERO
-    out[(u >= 0.02) & (u < 0.03)] = pinf
-    out[(u >= 0.03) & (u < 0.04)] = ninf
+        out[...] = base
+        return
+    blk = base.copy()
+    u = (words(seed, 2, n, start, 1) >> sh).astype(np.float64).reshape(rows, cols) * (2.0 ** -53)
+    nan_sign = (words(seed, 3, n, start, 1) & np.uint64(1)).reshape(rows, cols).astype(bool)
+    src_col = (words(seed, 4, n, start, 1) % np.uint64(cols)).astype(np.int64).reshape(rows, cols)
+    blk[u < 0.01] = F16_PZERO
+    blk[(u >= 0.01) & (u < 0.02)] = F16_NZERO
+    blk[(u >= 0.02) & (u < 0.03)] = pinf
+    blk[(u >= 0.03) & (u < 0.04)] = ninf
     nan = (u >= 0.04) & (u < 0.05)
-    out[nan & ~nan_sign] = pnan
-    out[nan & nan_sign] = nnan
+    blk[nan & ~nan_sign] = pnan
+    blk[nan & nan_sign] = nnan
     dup = (u >= 0.05) & (u < 0.15)
     r_idx = np.broadcast_to(np.arange(rows)[:, None], (rows, cols))
-    out[dup] = base[r_idx[dup], src_col[dup]]
+    blk[dup] = base[r_idx[dup], src_col[dup]]
+    out[...] = blk
+
+
+def rows16(rows: int, cols: int, kind: str = "f16", seed: int = 0,
+           specials: bool = True, threads: int | None = None) -> np.ndarray:
+    """(rows, cols) uint16 bit patterns of fp16 ("f16") or bf16 ("bf16") values.
+
+    Base value: standard normal by Box-Muller from two 53-bit uniforms
+    (streams 0 and 1), rounded to the format nearest-even.  With ``specials``:
+    for u = w(seed, 2, i) * 2**-64, [0,.01) +0, [.01,.02) -0, [.02,.03) +inf,
+    [.03,.04) -inf, [.04,.05) NaN (sign = bit 0 of w(seed, 3, i)) and
+    [.05,.15) a copy of the base value at column w(seed, 4, i) mod cols of the
+    same row.  i is the flat row-major index.
+    """
+    if kind not in ("f16", "bf16"):
+        raise ValueError("kind must be 'f16' or 'bf16'")
+    out = np.empty((rows, cols), np.uint16)
+    if rows == 0 or cols == 0:
+        return out
+    per = max(1, (1 << 20) // max(cols, 1))
+    blocks = [(r, min(per, rows - r)) for r in range(0, rows, per)]
+    threads = threads or min(16, os.cpu_count() or 1)
+    if len(blocks) == 1:
+        _rows16_block(out, 0, rows, cols, kind, seed, specials)
+        return out
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda b: _rows16_block(out[b[0]:b[0] + b[1]], b[0], b[1], cols, kind,
+                                            seed, specials), blocks))
     return out

@@ -23,3 +23,13 @@ def read_golden(name):
             k, v = line.split(":", 1)
             out[k.strip()] = [int(t) for t in v.split()]
     return out
+
+
+@pytest.fixture(scope="session")
+def rs():
+    """The CUDA library, built for sm_103a and loaded (GPU tests only)."""
+    from lsd_radix_sort_gb300 import build
+    build.build()
+    import lsd_radix_sort_gb300 as mod
+    mod.load_library()
+    return mod
