@@ -55,7 +55,8 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIB
+    """The in-tree library, or the one named by LSDRS_LIB (tuning builds)."""
+    return os.environ.get("LSDRS_LIB") or _build.LIB
 
 
 def load_library() -> ctypes.CDLL:

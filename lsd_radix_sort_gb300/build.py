@@ -56,16 +56,21 @@ def up_to_date() -> bool:
     return os.path.exists(LIB) and os.path.getmtime(LIB) >= _deps_mtime()
 
 
-def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None) -> str:
-    if not force and up_to_date():
+def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None,
+          defines: list[str] | None = None, out: str | None = None) -> str:
+    """Compile and link; ``defines``/``out`` build a variant library elsewhere."""
+    lib = out or LIB
+    if not force and not defines and out is None and up_to_date():
         return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    bdir = os.path.dirname(lib) if out else BUILD
+    os.makedirs(bdir, exist_ok=True)
+    dflags = [f"-D{d}" for d in (defines or [])]
     srcs = sources()
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
 
     def compile_one(src: str):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *dflags, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r
 
@@ -78,21 +83,24 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = N
             sys.stderr.write(f"== {os.path.basename(s)}\n{r.stdout}{r.stderr}")
     if failed:
         raise RuntimeError("nvcc failed for: " + ", ".join(os.path.basename(s) for s, _ in failed))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     libdir = cuda_lib_dir()
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp,
            *[o for _, o, _ in results], "-Xlinker", f"-rpath,{libdir}"]
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
     ap.add_argument("--verbose-ptxas", action="store_true")
+    ap.add_argument("-D", dest="defines", action="append", default=[])
+    ap.add_argument("--out", default=None)
     args = ap.parse_args()
-    print(build(force=args.force, verbose_ptxas=args.verbose_ptxas))
+    print(build(force=args.force, verbose_ptxas=args.verbose_ptxas, defines=args.defines,
+                out=args.out))
 
 
 if __name__ == "__main__":

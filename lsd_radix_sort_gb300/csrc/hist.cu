@@ -8,9 +8,8 @@
 // row in one sweep).  Counting uses shared-memory counters private to the
 // CTA ("privatized" histograms, CUDA Handbook ch. 16 section 16.3, named in
 // the Radix Sort section as usable without modification), replicated over
-// kCols lane columns so that equal digits in one warp hit at most
-// 32 / kCols copies, plus run-length merging of equal consecutive digits per
-// thread so that skewed and constant inputs do not serialise on one counter.
+// lane columns so that a warp's increments never serialise on one counter,
+// whatever the key distribution.
 // Each CTA writes its partial counts to its own slot; K-SCAN adds the slots
 // and scans (DSA CUDA from First Principles, section 13.1: the base of digit
 // d is the exclusive prefix sum of the counts of the digits below it).
@@ -22,13 +21,16 @@ namespace lsdrs {
 
 namespace {
 
-constexpr int kCols = 8;
-
+// Counter columns per digit: lane l counts into column l % kCols.  With 32
+// columns every lane of a warp owns its own column and bank, so a warp's 32
+// increments never collide, whatever the digits are (constant input included).
+// 16 columns when 32 would not fit in shared memory (64-bit keys, 8-bit digits).
 template <class KeyOp, int BITS>
 struct HistCfg {
   static constexpr int kRadix = 1 << BITS;
   static constexpr int kMaxPasses = (KeyOp::kBits + BITS - 1) / BITS;
-  static constexpr bool kMerge = kMaxPasses <= 8;
+  static constexpr int kCols =
+      static_cast<size_t>(kMaxPasses) * kRadix * 32 * sizeof(uint32_t) <= 128 * 1024 ? 32 : 16;
   static constexpr int kVec = 16 / sizeof(typename KeyOp::T);
   static constexpr int kUnroll = 4;
   static size_t smem_bytes(int passes) {
@@ -37,70 +39,34 @@ struct HistCfg {
 };
 
 template <class KeyOp, int BITS>
-struct Counter {
+__device__ __forceinline__ void count_key(uint32_t* cnt_col, typename KeyOp::T k, int begin_bit,
+                                          int passes, uint32_t last_mask, uint32_t flip) {
   using Cfg = HistCfg<KeyOp, BITS>;
-  static constexpr int R = Cfg::kRadix;
-  static constexpr int MP = Cfg::kMerge ? Cfg::kMaxPasses : 1;
-  uint32_t* cnt;
-  uint32_t col;
-  int begin_bit, passes;
-  uint32_t last_mask, flip;
-  uint32_t cur_d[MP];
-  uint32_t cur_c[MP];
-
-  __device__ __forceinline__ void init() {
+  constexpr int R = Cfg::kRadix;
+  constexpr int C = Cfg::kCols;
 #pragma unroll
-    for (int p = 0; p < MP; ++p) {
-      cur_d[p] = 0;
-      cur_c[p] = 0;
+  for (int p = 0; p < Cfg::kMaxPasses; ++p) {
+    if (p < passes) {
+      const uint32_t mask = p == passes - 1 ? last_mask : static_cast<uint32_t>(R - 1);
+      const uint32_t d = KeyOp::digit(k, begin_bit + p * BITS, mask, flip);
+      atomicAdd(cnt_col + (p * R + d) * C, 1u);
     }
   }
-  __device__ __forceinline__ uint32_t mask_of(int p) const {
-    return p == passes - 1 ? last_mask : static_cast<uint32_t>(R - 1);
-  }
-  __device__ __forceinline__ void add(typename KeyOp::T k) {
-    if constexpr (Cfg::kMerge) {
-#pragma unroll
-      for (int p = 0; p < MP; ++p) {
-        if (p < passes) {
-          uint32_t d = KeyOp::digit(k, begin_bit + p * BITS, mask_of(p), flip);
-          if (d == cur_d[p]) {
-            cur_c[p] += 1;
-          } else {
-            if (cur_c[p]) atomicAdd(&cnt[(p * R + cur_d[p]) * kCols + col], cur_c[p]);
-            cur_d[p] = d;
-            cur_c[p] = 1;
-          }
-        }
-      }
-    } else {
-      for (int p = 0; p < passes; ++p) {
-        uint32_t d = KeyOp::digit(k, begin_bit + p * BITS, mask_of(p), flip);
-        atomicAdd(&cnt[(p * R + d) * kCols + col], 1u);
-      }
-    }
-  }
-  __device__ __forceinline__ void flush() {
-    if constexpr (Cfg::kMerge) {
-#pragma unroll
-      for (int p = 0; p < MP; ++p)
-        if (p < passes && cur_c[p]) atomicAdd(&cnt[(p * R + cur_d[p]) * kCols + col], cur_c[p]);
-    }
-  }
-};
+}
 
 template <class KeyOp, int BITS>
-__global__ void __launch_bounds__(kHistThreads) upfront_hist_kernel(HistArgs a) {
+__global__ void __launch_bounds__(kHistThreads, 1) upfront_hist_kernel(HistArgs a) {
   using T = typename KeyOp::T;
   using Cfg = HistCfg<KeyOp, BITS>;
   constexpr int R = Cfg::kRadix;
+  constexpr int C = Cfg::kCols;
   constexpr int V = Cfg::kVec;
   constexpr int U = Cfg::kUnroll;
   extern __shared__ __align__(16) uint32_t cnt[];
 
   const int tid = threadIdx.x;
   const int nb = a.passes * R;
-  for (int i = tid; i < nb * kCols; i += kHistThreads) cnt[i] = 0;
+  for (int i = tid; i < nb * C; i += kHistThreads) cnt[i] = 0;
 
   // Zero the look-back words and counters the sweeps start from.
   {
@@ -116,15 +82,9 @@ __global__ void __launch_bounds__(kHistThreads) upfront_hist_kernel(HistArgs a) 
   const int64_t begin = static_cast<int64_t>(chunk) * a.chunk_len;
   const int64_t end = begin + a.chunk_len < a.cols ? begin + a.chunk_len : a.cols;
   const T* base = static_cast<const T*>(a.keys) + row * a.cols;
-
-  Counter<KeyOp, BITS> c;
-  c.cnt = cnt;
-  c.col = tid & (kCols - 1);
-  c.begin_bit = a.begin_bit;
-  c.passes = a.passes;
-  c.last_mask = a.last_mask;
-  c.flip = a.flip;
-  c.init();
+  uint32_t* col = cnt + (tid & (C - 1));
+  const int begin_bit = a.begin_bit, passes = a.passes;
+  const uint32_t last_mask = a.last_mask, flip = a.flip;
 
   if (begin < end) {
     // Split [begin, end) into a scalar head up to 16-byte alignment, a
@@ -135,38 +95,38 @@ __global__ void __launch_bounds__(kHistThreads) upfront_hist_kernel(HistArgs a) 
     const int64_t body_begin = begin + head;
     const int64_t nvec = (end - body_begin) / V;
     const int64_t body_end = body_begin + nvec * V;
-    if (tid < head) c.add(base[begin + tid]);
-    if (tid < end - body_end) c.add(base[body_end + tid]);
+    if (tid < head) count_key<KeyOp, BITS>(col, base[begin + tid], begin_bit, passes, last_mask, flip);
+    if (tid < end - body_end)
+      count_key<KeyOp, BITS>(col, base[body_end + tid], begin_bit, passes, last_mask, flip);
 
-    using Vec = uint4;
-    const Vec* vp = reinterpret_cast<const Vec*>(base + body_begin);
+    const uint4* vp = reinterpret_cast<const uint4*>(base + body_begin);
     int64_t v = tid;
     for (; v + (U - 1) * kHistThreads < nvec; v += U * kHistThreads) {
-      Vec buf[U];
+      uint4 buf[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) buf[u] = __ldcs(vp + v + u * kHistThreads);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const T* ks = reinterpret_cast<const T*>(&buf[u]);
 #pragma unroll
-        for (int e = 0; e < V; ++e) c.add(ks[e]);
+        for (int e = 0; e < V; ++e)
+          count_key<KeyOp, BITS>(col, ks[e], begin_bit, passes, last_mask, flip);
       }
     }
     for (; v < nvec; v += kHistThreads) {
-      Vec b = __ldcs(vp + v);
+      uint4 b = __ldcs(vp + v);
       const T* ks = reinterpret_cast<const T*>(&b);
 #pragma unroll
-      for (int e = 0; e < V; ++e) c.add(ks[e]);
+      for (int e = 0; e < V; ++e) count_key<KeyOp, BITS>(col, ks[e], begin_bit, passes, last_mask, flip);
     }
   }
-  c.flush();
   __syncthreads();
 
   uint32_t* slot = a.slots + (row * a.chunks_per_row + chunk) * static_cast<int64_t>(nb);
   for (int b = tid; b < nb; b += kHistThreads) {
     uint32_t s = 0;
 #pragma unroll
-    for (int k = 0; k < kCols; ++k) s += cnt[b * kCols + k];
+    for (int k = 0; k < C; ++k) s += cnt[b * C + (k + b) % C];
     slot[b] = s;
   }
 }

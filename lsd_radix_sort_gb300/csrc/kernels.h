@@ -18,21 +18,49 @@ enum ValKind { kValNone = 0, kValU32 = 1, kValIdx = 2 };
 struct SweepShape {
   int threads;
   int items;
+  int min_blocks;  // resident CTAs per SM the register budget is sized for
   constexpr int tile() const { return threads * items; }
 };
-constexpr SweepShape kShapeU32Keys{512, 16};
-constexpr SweepShape kShapeU32Pairs{512, 12};
-constexpr SweepShape kShapeU64Keys{512, 8};
-constexpr SweepShape kShapeU64Pairs{512, 8};
-constexpr SweepShape kShapeF16Idx{512, 8};
-constexpr int kSweepMinBlocks = 2;
+// Shapes may be overridden at build time for tuning sweeps, e.g.
+// -DLSDRS_U32P_T=256 -DLSDRS_U32P_I=16 -DLSDRS_U32P_B=4 (threads, items per
+// thread, CTAs per SM); the defaults are the measured best on GB300.
+#ifndef LSDRS_U32K_T
+#define LSDRS_U32K_T 512
+#define LSDRS_U32K_I 16
+#define LSDRS_U32K_B 2
+#endif
+#ifndef LSDRS_U32P_T
+#define LSDRS_U32P_T 512
+#define LSDRS_U32P_I 12
+#define LSDRS_U32P_B 2
+#endif
+#ifndef LSDRS_U64K_T
+#define LSDRS_U64K_T 512
+#define LSDRS_U64K_I 8
+#define LSDRS_U64K_B 2
+#endif
+#ifndef LSDRS_U64P_T
+#define LSDRS_U64P_T 512
+#define LSDRS_U64P_I 8
+#define LSDRS_U64P_B 2
+#endif
+#ifndef LSDRS_F16_T
+#define LSDRS_F16_T 512
+#define LSDRS_F16_I 8
+#define LSDRS_F16_B 2
+#endif
+constexpr SweepShape kShapeU32Keys{LSDRS_U32K_T, LSDRS_U32K_I, LSDRS_U32K_B};
+constexpr SweepShape kShapeU32Pairs{LSDRS_U32P_T, LSDRS_U32P_I, LSDRS_U32P_B};
+constexpr SweepShape kShapeU64Keys{LSDRS_U64K_T, LSDRS_U64K_I, LSDRS_U64K_B};
+constexpr SweepShape kShapeU64Pairs{LSDRS_U64P_T, LSDRS_U64P_I, LSDRS_U64P_B};
+constexpr SweepShape kShapeF16Idx{LSDRS_F16_T, LSDRS_F16_I, LSDRS_F16_B};
 constexpr SweepShape sweep_shape(KeyKind k, ValKind v) {
   return k == kKeyU32 ? (v == kValNone ? kShapeU32Keys : kShapeU32Pairs)
        : k == kKeyU64 ? (v == kValNone ? kShapeU64Keys : kShapeU64Pairs)
                       : kShapeF16Idx;
 }
 
-constexpr int kHistThreads = 512;
+constexpr int kHistThreads = 1024;
 constexpr int kHistTargetCtas = 608;   // 152 SMs x 4 resident CTAs
 constexpr int64_t kHistMinChunk = 4096;
 constexpr int kScanThreads = 256;

@@ -10,7 +10,9 @@
 //  1. The tile index comes from an atomic counter, so tiles start in index
 //     order and every tile a CTA waits on belongs to a CTA that is already
 //     running (forward progress of the look-back).
-//  2. Keys are loaded warp-striped: warp w owns a contiguous run of 32*ITEMS
+//  2. The tile's payloads are requested at once with one bulk (TMA) copy into
+//     shared memory; they are not needed before step 7.  Keys are loaded
+//     warp-striped into registers: warp w owns a contiguous run of 32*ITEMS
 //     keys and its item i covers keys 32*i .. 32*i+31 of that run, one per
 //     lane, so (warp, item, lane) order is input order.
 //  3. Rank within the warp: for each item, the lanes holding the same digit
@@ -25,56 +27,142 @@
 //     digit's start inside the tile.
 //  5. Keys are placed in shared memory in tile-sorted order.
 //  6. Look-back: for each digit, the counts of earlier tiles of the row are
-//     summed walking backwards until a tile that has published its inclusive
-//     prefix (flag P); this tile then publishes its own inclusive prefix.
-//     The precomputed alternative (per-tile offsets from a separate pass,
-//     FlagTree PR #1084 section 2) needs a second read of the keys; the
-//     look-back needs none.  Every wait is bounded in time.
+//     summed walking backwards, a window of tiles per memory round trip,
+//     until a tile that has published its inclusive prefix (flag P); this
+//     tile then publishes its own inclusive prefix.  The precomputed
+//     alternative (per-tile offsets from a separate pass, FlagTree PR #1084
+//     section 2) needs a second read of the keys; the look-back needs none.
+//     Every wait is bounded in time.
 //  7. Thread j writes staged key j to base[d] + prefix[d] + (j - start[d]):
 //     every digit's keys leave as one contiguous run ("100 Days of GPU",
 //     day 35: after the local sort the write out is one run per digit).
 //     Payloads follow through the same staging buffer.
 // Lanes past the end of the last tile take the highest digit, rank after
 // every real key of the tile, are not counted in the published counts and
-// are not stored (the page's sentinel padding, without the padding).
+// are not stored (the page's sentinel padding, without the padding).  Full
+// tiles run a separate instantiation with no bounds checks.
 #pragma once
 #include "common.cuh"
 #include "kernels.h"
 #include "keys.cuh"
 
+// Tuning knobs (build-time): predecessor words read per look-back round
+// trip, a sleep between polls of a word that is not ready, the hardware
+// match instruction instead of per-bit ballots, the bulk copy of payloads,
+// and look-back statistics for measurement builds.
+#ifndef LSDRS_LOOKBACK_WINDOW
+#define LSDRS_LOOKBACK_WINDOW 16
+#endif
+#ifndef LSDRS_SPIN_SLEEP_NS
+#define LSDRS_SPIN_SLEEP_NS 0
+#endif
+#ifndef LSDRS_MATCH_ANY
+#define LSDRS_MATCH_ANY 0
+#endif
+#ifndef LSDRS_VALS_TMA
+#define LSDRS_VALS_TMA 1
+#endif
+#ifndef LSDRS_STATS
+#define LSDRS_STATS 0
+#endif
+
 namespace lsdrs {
+
+// Header words of the scratch buffer that measurement builds accumulate
+// look-back statistics into (look-back round trips, polls of unready words).
+constexpr int kStatsWord = 100;
 
 // Lanes of the warp whose digit equals this lane's digit.
 template <int BITS>
 __device__ __forceinline__ uint32_t digit_peers(uint32_t d) {
+#if LSDRS_MATCH_ANY
+  return __match_any_sync(kFull, d);
+#else
   uint32_t peers = kFull;
 #pragma unroll
   for (int b = 0; b < BITS; ++b) {
-    const bool bit = (d >> b) & 1u;
-    const uint32_t votes = __ballot_sync(kFull, bit);
-    peers &= bit ? votes : ~votes;
+    // m: all ones when bit b of d is set; the peers agree with m on bit b.
+    const uint32_t m = static_cast<uint32_t>(static_cast<int32_t>(d << (31 - b)) >> 31);
+    const uint32_t votes = __ballot_sync(kFull, m);
+    peers &= ~(votes ^ m);
   }
   return peers;
+#endif
 }
 
 // Bounded wait for a non-zero look-back word.  On timeout, or when another
 // tile has already reported an error, records the error and returns a word
 // with flag P and value 0 so that the walk ends.
 __device__ __forceinline__ uint32_t wait_status(const uint32_t* p, uint32_t* error,
-                                                uint64_t timeout_ns) {
+                                                uint64_t timeout_ns, uint32_t& polls) {
   uint32_t v = ld_relaxed(p);
   if (v != 0) return v;
   const uint64_t t0 = global_timer_ns();
   uint32_t spins = 0;
   for (;;) {
+#if LSDRS_SPIN_SLEEP_NS > 0
+    __nanosleep(LSDRS_SPIN_SLEEP_NS);
+#endif
     v = ld_relaxed(p);
-    if (v != 0) return v;
-    if ((++spins & 63u) == 0) {
-      if (ld_relaxed(error) != kErrNone) return kFlagP;
+    ++spins;
+    if (v != 0) break;
+    if ((spins & 63u) == 0) {
+      if (ld_relaxed(error) != kErrNone) {
+        v = kFlagP;
+        break;
+      }
       if (global_timer_ns() - t0 > timeout_ns) {
         atomicCAS(error, kErrNone, kErrLookback);
-        return kFlagP;
+        v = kFlagP;
+        break;
       }
+    }
+  }
+  polls += spins;
+  return v;
+}
+
+// Exclusive prefix of one digit over tiles [0, t) of a row.  `col` points at
+// this digit's word of the row's tile 0; tile k's word is col[k * R].  Each
+// round trip loads the words of WIN predecessors at once (for the 32 digits
+// of a warp these are coalesced 128-byte rows) and consumes them up to the
+// first inclusive prefix, or up to the first word not yet published, on
+// which it then waits.
+template <int R>
+__device__ __forceinline__ uint32_t look_back(const uint32_t* col, int64_t t, uint32_t* error,
+                                              uint64_t timeout_ns, uint32_t& trips,
+                                              uint32_t& polls) {
+  constexpr int WIN = LSDRS_LOOKBACK_WINDOW;
+  static_assert(WIN >= 1 && WIN <= 32, "window of 1..32 tiles");
+  uint32_t excl = 0;
+  int64_t pt = t - 1;  // newest predecessor not yet consumed
+  for (;;) {
+    uint32_t v[WIN];
+#pragma unroll
+    for (int k = 0; k < WIN; ++k) v[k] = (pt - k >= 0) ? ld_relaxed(col + (pt - k) * R) : kFlagP;
+    ++trips;
+    uint32_t zero_mask = 0, p_mask = 0;
+#pragma unroll
+    for (int k = 0; k < WIN; ++k) {
+      zero_mask |= (v[k] == 0 ? 1u : 0u) << k;
+      p_mask |= (v[k] >> 31) << k;
+    }
+    // consume words [0, stop): up to and including the first P, or up to
+    // (not including) the first unpublished word, whichever comes first.
+    const int first_p = p_mask ? __ffs(p_mask) - 1 : WIN;
+    const int first_zero = zero_mask ? __ffs(zero_mask) - 1 : WIN;
+    const bool done = first_p < first_zero;
+    const int stop = done ? first_p + 1 : first_zero;
+#pragma unroll
+    for (int k = 0; k < WIN; ++k) excl += (k < stop) ? (v[k] & kValueMask) : 0u;
+    if (done) return excl;
+    if (first_zero < WIN) {
+      const uint32_t w = wait_status(col + (pt - first_zero) * R, error, timeout_ns, polls);
+      excl += w & kValueMask;
+      if (w & kFlagP) return excl;
+      pt -= first_zero + 1;
+    } else {
+      pt -= WIN;
     }
   }
 }
@@ -85,96 +173,79 @@ struct SweepSmem {
   static constexpr int kRadix = 1 << BITS;
   static constexpr int kWarps = THREADS / kWarp;
   static constexpr int kTile = THREADS * ITEMS;
-  using V = uint32_t;  // staged payload word (u32 or int32 index)
+  static constexpr bool kVals = VK != kValNone;
   static constexpr size_t kStageBytes =
-      (VK != kValNone && sizeof(V) > sizeof(T)) ? kTile * sizeof(V) : kTile * sizeof(T);
+      (kVals && sizeof(uint32_t) > sizeof(T)) ? kTile * sizeof(uint32_t) : kTile * sizeof(T);
   alignas(16) unsigned char stage[kStageBytes];
+  alignas(16) uint32_t vin[kVals ? kTile : 4];  // the tile's payloads, input order
   uint32_t warp_cnt[kWarps][kRadix];
   uint32_t tile_start[kRadix];
   uint32_t g_off[kRadix];
+  uint64_t bar;
   uint32_t tile_id;
   uint32_t abort;
 };
 
-template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB>
-__global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
+template <bool FULL, class KeyOp, int BITS, int VK, int THREADS, int ITEMS>
+__device__ __forceinline__ void sweep_tile(const SweepArgs& a,
+                                           SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>& s,
+                                           int64_t tile, int64_t row, int64_t t, int valid) {
   using T = typename KeyOp::T;
   using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
   constexpr int R = S::kRadix;
   constexpr int W = S::kWarps;
   constexpr int TILE = S::kTile;
   constexpr int WKEYS = kWarp * ITEMS;
-  static_assert(R <= THREADS, "one thread per digit");
-
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  S& s = *reinterpret_cast<S*>(smem_raw);
+  constexpr bool kVals = S::kVals;
   T* stage_keys = reinterpret_cast<T*>(s.stage);
   uint32_t* stage_vals = reinterpret_cast<uint32_t*>(s.stage);
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int warp = tid >> 5;
-
-  if (tid == 0) {
-    s.tile_id = atomicAdd(a.tile_counter, 1u);
-    s.abort = ld_relaxed(a.error) != kErrNone;
-  }
-  for (int i = tid; i < W * R; i += THREADS) (&s.warp_cnt[0][0])[i] = 0;
-  __syncthreads();
-
-  const int64_t tile = s.tile_id;
-  const int64_t row = tile / a.tiles_per_row;
-  const int64_t t = tile - row * a.tiles_per_row;
   const int64_t row_base = row * a.cols;
   const int64_t tile_begin = t * TILE;
-  const int valid = static_cast<int>(a.cols - tile_begin < TILE ? a.cols - tile_begin : TILE);
   uint32_t* status_tile = a.status + tile * R;
-
-  if (s.abort) {  // an earlier tile failed: release successors and stop
-    if (tid < R) st_relaxed(status_tile + tid, kFlagP);
-    if (a.status_zero != nullptr && tid < R) a.status_zero[tile * R + tid] = 0;
-    return;
-  }
-
-  // ---- 2. load (warp-striped) -------------------------------------------
   const int wpos = warp * WKEYS + lane;  // tile position of item 0
-  const T* kin = static_cast<const T*>(a.keys_in) + row_base + tile_begin + wpos;
-  T keys[ITEMS];
-  if (valid == TILE) {
-#pragma unroll
-    for (int i = 0; i < ITEMS; ++i) keys[i] = ld_stream(kin + i * kWarp);
-  } else {
-#pragma unroll
-    for (int i = 0; i < ITEMS; ++i)
-      keys[i] = (wpos + i * kWarp < valid) ? ld_stream(kin + i * kWarp) : T(0);
-  }
-  uint32_t vals[VK == kValNone ? 1 : ITEMS];
-  if constexpr (VK != kValNone) {
-    if (VK == kValIdx && a.vals_in == nullptr) {
-#pragma unroll
-      for (int i = 0; i < ITEMS; ++i) vals[i] = static_cast<uint32_t>(tile_begin + wpos + i * kWarp);
-    } else {
-      const uint32_t* vin = static_cast<const uint32_t*>(a.vals_in) + row_base + tile_begin + wpos;
-      if (valid == TILE) {
-#pragma unroll
-        for (int i = 0; i < ITEMS; ++i) vals[i] = ld_stream(vin + i * kWarp);
+  const bool gen_idx = VK == kValIdx && a.vals_in == nullptr;
+  uint32_t trips = 0, polls = 0;
+
+  // ---- 2. payloads -> shared memory (bulk copy), keys -> registers -------
+  bool vals_tma = false;
+  if constexpr (kVals) {
+    if (!gen_idx) {
+      const uint32_t* src = static_cast<const uint32_t*>(a.vals_in) + row_base + tile_begin;
+      vals_tma = FULL && LSDRS_VALS_TMA && (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+      if (vals_tma) {
+        if (tid == 0) {
+          mbar_init(&s.bar, 1);
+          mbar_arrive_expect_tx(&s.bar, TILE * sizeof(uint32_t));
+          bulk_copy_g2s(s.vin, src, TILE * sizeof(uint32_t), &s.bar);
+        }
       } else {
 #pragma unroll
         for (int i = 0; i < ITEMS; ++i)
-          vals[i] = (wpos + i * kWarp < valid) ? ld_stream(vin + i * kWarp) : 0u;
+          if (FULL || wpos + i * kWarp < valid)
+            s.vin[wpos + i * kWarp] = ld_stream(src + wpos + i * kWarp);
       }
     }
   }
+  const T* kin = static_cast<const T*>(a.keys_in) + row_base + tile_begin + wpos;
+  T keys[ITEMS];
+#pragma unroll
+  for (int i = 0; i < ITEMS; ++i)
+    keys[i] = (FULL || wpos + i * kWarp < valid) ? ld_stream(kin + i * kWarp) : T(0);
 
   // ---- 3. rank within the warp ------------------------------------------
   // packed[i] = digit << 16 | rank of the item among the warp's keys of
   // that digit.
   uint32_t packed[ITEMS];
   uint32_t* wc = s.warp_cnt[warp];
+  const uint32_t lt = lanemask_lt();
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
-    const uint32_t d = (wpos + i * kWarp < valid) ? KeyOp::digit(keys[i], a.shift, a.mask, a.flip)
-                                                  : static_cast<uint32_t>(R - 1);
+    uint32_t d = KeyOp::digit(keys[i], a.shift, a.mask, a.flip);
+    if (!FULL && wpos + i * kWarp >= valid) d = R - 1;
     const uint32_t peers = digit_peers<BITS>(d);
     const int leader = __ffs(peers) - 1;
     uint32_t before = 0;
@@ -184,7 +255,7 @@ __global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
     }
     before = __shfl_sync(kFull, before, leader);
     __syncwarp();
-    packed[i] = (d << 16) | (before + __popc(peers & lanemask_lt()));
+    packed[i] = (d << 16) | (before + __popc(peers & lt));
   }
   __syncthreads();
 
@@ -199,7 +270,7 @@ __global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
       sum += c;
     }
     s.tile_start[tid] = sum;
-    my_count = (tid == R - 1) ? sum - static_cast<uint32_t>(TILE - valid) : sum;
+    my_count = (!FULL && tid == R - 1) ? sum - static_cast<uint32_t>(TILE - valid) : sum;
     st_relaxed(status_tile + tid, (t == 0 ? kFlagP : kFlagA) | my_count);
   }
   __syncthreads();
@@ -242,55 +313,97 @@ __global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
   if (tid < R) {
     uint32_t excl = 0;
     if (t > 0) {
-      const uint32_t* p = status_tile - R + tid;
-      for (;;) {
-        const uint32_t v = wait_status(p, a.error, a.timeout_ns);
-        excl += v & kValueMask;
-        if (v & kFlagP) break;
-        p -= R;
-      }
+      excl = look_back<R>(a.status + (tile - t) * R + tid, t, a.error, a.timeout_ns, trips, polls);
       st_relaxed(status_tile + tid, kFlagP | (excl + my_count));
     }
     s.g_off[tid] = a.bases[row * a.bases_row_stride + tid] + excl - s.tile_start[tid];
   }
+#if LSDRS_STATS
+  if (trips) atomicAdd(a.error + kStatsWord, trips);
+  if (polls) atomicAdd(a.error + kStatsWord + 1, polls);
+#endif
   __syncthreads();
 
   // ---- 7. contiguous per-digit runs out ---------------------------------
   T* kout = static_cast<T*>(a.keys_out) + row_base;
-  uint32_t dst[VK == kValNone ? 1 : ITEMS];
+  uint32_t dst[kVals ? ITEMS : 1];
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
     const int j = i * THREADS + tid;
-    if (j < valid) {
+    if (FULL || j < valid) {
       const T k = stage_keys[j];
       const uint32_t d = KeyOp::digit(k, a.shift, a.mask, a.flip);
       const uint32_t g = s.g_off[d] + static_cast<uint32_t>(j);
       kout[g] = k;
-      if constexpr (VK != kValNone) dst[i] = g;
+      if constexpr (kVals) dst[i] = g;
     }
   }
-  if constexpr (VK != kValNone) {
-    __syncthreads();
+  if constexpr (kVals) {
+    if (vals_tma && !mbar_wait_bounded(&s.bar, 0, a.timeout_ns)) {
+      atomicCAS(a.error, kErrNone, kErrLookback);
+      mbar_wait_bounded(&s.bar, 0, a.timeout_ns);  // let the copy land before leaving
+      return;
+    }
+    __syncthreads();  // staged keys consumed; payloads visible
 #pragma unroll
-    for (int i = 0; i < ITEMS; ++i) stage_vals[packed[i]] = vals[i];
+    for (int i = 0; i < ITEMS; ++i) {
+      const uint32_t v = gen_idx ? static_cast<uint32_t>(tile_begin + wpos + i * kWarp)
+                                 : s.vin[wpos + i * kWarp];
+      stage_vals[packed[i]] = v;
+    }
     __syncthreads();
     if (VK == kValIdx && a.wide_out) {
       int64_t* vout = static_cast<int64_t*>(a.vals_out) + row_base;
 #pragma unroll
       for (int i = 0; i < ITEMS; ++i) {
         const int j = i * THREADS + tid;
-        if (j < valid) vout[dst[i]] = static_cast<int64_t>(static_cast<int32_t>(stage_vals[j]));
+        if (FULL || j < valid)
+          vout[dst[i]] = static_cast<int64_t>(static_cast<int32_t>(stage_vals[j]));
       }
     } else {
       uint32_t* vout = static_cast<uint32_t*>(a.vals_out) + row_base;
 #pragma unroll
       for (int i = 0; i < ITEMS; ++i) {
         const int j = i * THREADS + tid;
-        if (j < valid) vout[dst[i]] = stage_vals[j];
+        if (FULL || j < valid) vout[dst[i]] = stage_vals[j];
       }
     }
   }
+}
 
+template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB>
+__global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
+  using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
+  constexpr int R = S::kRadix;
+  constexpr int W = S::kWarps;
+  constexpr int TILE = S::kTile;
+  static_assert(R <= THREADS, "one thread per digit");
+  static_assert(kWarp * ITEMS < 65536, "ranks are packed in 16 bits");
+
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  S& s = *reinterpret_cast<S*>(smem_raw);
+  const int tid = threadIdx.x;
+
+  if (tid == 0) {
+    s.tile_id = atomicAdd(a.tile_counter, 1u);
+    s.abort = ld_relaxed(a.error) != kErrNone;
+  }
+  for (int i = tid; i < W * R; i += THREADS) (&s.warp_cnt[0][0])[i] = 0;
+  __syncthreads();
+
+  const int64_t tile = s.tile_id;
+  const int64_t row = tile / a.tiles_per_row;
+  const int64_t t = tile - row * a.tiles_per_row;
+  const int64_t tile_begin = t * TILE;
+  const int valid = static_cast<int>(a.cols - tile_begin < TILE ? a.cols - tile_begin : TILE);
+
+  if (s.abort) {  // an earlier tile failed: release successors and stop
+    if (tid < R) st_relaxed(a.status + tile * R + tid, kFlagP);
+  } else if (valid == TILE) {
+    sweep_tile<true>(a, s, tile, row, t, valid);
+  } else {
+    sweep_tile<false>(a, s, tile, row, t, valid);
+  }
   if (a.status_zero != nullptr && tid < R) a.status_zero[tile * R + tid] = 0;
 }
 
