@@ -46,13 +46,10 @@
 #include "kernels.h"
 #include "keys.cuh"
 
-// Tuning knobs (build-time): predecessor words read per look-back round
-// trip, a sleep between polls of a word that is not ready, the hardware
+// Tuning knobs (build-time): a sleep between polls of a word that is not
+// ready, the hardware
 // match instruction instead of per-bit ballots, the bulk copy of payloads,
 // and look-back statistics for measurement builds.
-#ifndef LSDRS_LOOKBACK_WINDOW
-#define LSDRS_LOOKBACK_WINDOW 16
-#endif
 #ifndef LSDRS_SPIN_SLEEP_NS
 #define LSDRS_SPIN_SLEEP_NS 0
 #endif
@@ -69,8 +66,26 @@
 namespace lsdrs {
 
 // Header words of the scratch buffer that measurement builds accumulate
-// look-back statistics into (look-back round trips, polls of unready words).
+// look-back statistics into (look-back round trips, polls of unready words),
+// and, with LSDRS_STATS >= 2, per-phase cycle sums of thread 0 as 64-bit
+// counters from word kPhaseWord on.
 constexpr int kStatsWord = 100;
+constexpr int kPhaseWord = 104;
+#if LSDRS_STATS >= 2
+#define LSDRS_PHASE(k)                                                                   \
+  do {                                                                                   \
+    if (threadIdx.x == 0) {                                                              \
+      const long long now_ = clock64();                                                  \
+      atomicAdd(reinterpret_cast<unsigned long long*>(a.error + kPhaseWord) + (k),       \
+                static_cast<unsigned long long>(now_ - phase_t_));                       \
+      phase_t_ = now_;                                                                   \
+    }                                                                                    \
+  } while (0)
+#else
+#define LSDRS_PHASE(k) \
+  do {                 \
+  } while (0)
+#endif
 
 // Lanes of the warp whose digit equals this lane's digit.
 template <int BITS>
@@ -128,11 +143,10 @@ __device__ __forceinline__ uint32_t wait_status(const uint32_t* p, uint32_t* err
 // of a warp these are coalesced 128-byte rows) and consumes them up to the
 // first inclusive prefix, or up to the first word not yet published, on
 // which it then waits.
-template <int R>
+template <int R, int WIN>
 __device__ __forceinline__ uint32_t look_back(const uint32_t* col, int64_t t, uint32_t* error,
                                               uint64_t timeout_ns, uint32_t& trips,
                                               uint32_t& polls) {
-  constexpr int WIN = LSDRS_LOOKBACK_WINDOW;
   static_assert(WIN >= 1 && WIN <= 32, "window of 1..32 tiles");
   uint32_t excl = 0;
   int64_t pt = t - 1;  // newest predecessor not yet consumed
@@ -167,38 +181,37 @@ __device__ __forceinline__ uint32_t look_back(const uint32_t* col, int64_t t, ui
   }
 }
 
-template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS>
-struct SweepSmem {
-  using T = typename KeyOp::T;
-  static constexpr int kRadix = 1 << BITS;
-  static constexpr int kWarps = THREADS / kWarp;
-  static constexpr int kTile = THREADS * ITEMS;
-  static constexpr bool kVals = VK != kValNone;
-  static constexpr size_t kStageBytes =
-      (kVals && sizeof(uint32_t) > sizeof(T)) ? kTile * sizeof(uint32_t) : kTile * sizeof(T);
-  alignas(16) unsigned char stage[kStageBytes];
-  alignas(16) uint32_t vin[kVals ? kTile : 4];  // the tile's payloads, input order
-  uint32_t warp_cnt[kWarps][kRadix];
-  uint32_t tile_start[kRadix];
-  uint32_t g_off[kRadix];
-  uint64_t bar;
-  uint32_t tile_id;
-  uint32_t abort;
+// Shared-memory arrays every tile needs besides its key/payload buffers.
+template <int W, int R>
+struct TileScratch {
+  uint32_t warp_cnt[W][R];  // per-warp digit counters, then per-warp offsets
+  uint32_t tile_start[R];   // digit counts, then digit starts in the tile
+  uint32_t g_off[R];        // output position of staged slot j is g_off[d] + j
 };
 
-template <bool FULL, class KeyOp, int BITS, int VK, int THREADS, int ITEMS>
+// Where a tile's keys and payloads are read from and staged to.  Key and
+// payload sources are warp-striped: the item at tile position p is src[p].
+template <class KeyOp>
+struct TileIo {
+  const typename KeyOp::T* key_src;  // shared (prefetched) or global
+  const uint32_t* val_src;           // shared, global, or null (generate indices)
+  typename KeyOp::T* stage_keys;     // shared, TILE keys
+  uint32_t* stage_vals;              // shared, TILE words (may equal val_src)
+};
+
+// One tile: rank, publish, look back, stage, write.  Called by every thread
+// of the CTA; begins and ends with all threads converged.
+template <bool FULL, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
 __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
-                                           SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>& s,
-                                           int64_t tile, int64_t row, int64_t t, int valid) {
+                                           TileScratch<THREADS / kWarp, (1 << BITS)>& s,
+                                           const TileIo<KeyOp>& io, int64_t tile, int64_t row,
+                                           int64_t t, int valid) {
   using T = typename KeyOp::T;
-  using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
-  constexpr int R = S::kRadix;
-  constexpr int W = S::kWarps;
-  constexpr int TILE = S::kTile;
+  constexpr int R = 1 << BITS;
+  constexpr int W = THREADS / kWarp;
+  constexpr int TILE = THREADS * ITEMS;
   constexpr int WKEYS = kWarp * ITEMS;
-  constexpr bool kVals = S::kVals;
-  T* stage_keys = reinterpret_cast<T*>(s.stage);
-  uint32_t* stage_vals = reinterpret_cast<uint32_t*>(s.stage);
+  constexpr bool kVals = VK != kValNone;
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -207,34 +220,15 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   const int64_t tile_begin = t * TILE;
   uint32_t* status_tile = a.status + tile * R;
   const int wpos = warp * WKEYS + lane;  // tile position of item 0
-  const bool gen_idx = VK == kValIdx && a.vals_in == nullptr;
   uint32_t trips = 0, polls = 0;
+#if LSDRS_STATS >= 2
+  long long phase_t_ = clock64();
+#endif
 
-  // ---- 2. payloads -> shared memory (bulk copy), keys -> registers -------
-  bool vals_tma = false;
-  if constexpr (kVals) {
-    if (!gen_idx) {
-      const uint32_t* src = static_cast<const uint32_t*>(a.vals_in) + row_base + tile_begin;
-      vals_tma = FULL && LSDRS_VALS_TMA && (reinterpret_cast<uintptr_t>(src) & 15) == 0;
-      if (vals_tma) {
-        if (tid == 0) {
-          mbar_init(&s.bar, 1);
-          mbar_arrive_expect_tx(&s.bar, TILE * sizeof(uint32_t));
-          bulk_copy_g2s(s.vin, src, TILE * sizeof(uint32_t), &s.bar);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < ITEMS; ++i)
-          if (FULL || wpos + i * kWarp < valid)
-            s.vin[wpos + i * kWarp] = ld_stream(src + wpos + i * kWarp);
-      }
-    }
-  }
-  const T* kin = static_cast<const T*>(a.keys_in) + row_base + tile_begin + wpos;
   T keys[ITEMS];
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i)
-    keys[i] = (FULL || wpos + i * kWarp < valid) ? ld_stream(kin + i * kWarp) : T(0);
+    keys[i] = (FULL || wpos + i * kWarp < valid) ? io.key_src[wpos + i * kWarp] : T(0);
 
   // ---- 3. rank within the warp ------------------------------------------
   // packed[i] = digit << 16 | rank of the item among the warp's keys of
@@ -258,6 +252,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     packed[i] = (d << 16) | (before + __popc(peers & lt));
   }
   __syncthreads();
+  LSDRS_PHASE(0);  // loads + ranking
 
   // ---- 4. warp offsets, tile counts, publish, digit starts --------------
   uint32_t my_count = 0;  // this tile's count of digit tid (without padding)
@@ -274,6 +269,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     st_relaxed(status_tile + tid, (t == 0 ? kFlagP : kFlagA) | my_count);
   }
   __syncthreads();
+  LSDRS_PHASE(1);  // warp offsets + publish
   if (warp == 0) {  // exclusive scan of tile_start over the digits
     constexpr int PER = (R + kWarp - 1) / kWarp;
     uint32_t v[PER];
@@ -299,88 +295,237 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     }
   }
   __syncthreads();
+  LSDRS_PHASE(2);  // digit scan
 
-  // ---- 5. stage keys in tile-sorted order -------------------------------
+  // ---- 5. stage keys, then payloads, in tile-sorted order ---------------
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
     const uint32_t d = packed[i] >> 16;
     const uint32_t pos = s.tile_start[d] + s.warp_cnt[warp][d] + (packed[i] & 0xFFFFu);
-    stage_keys[pos] = keys[i];
+    io.stage_keys[pos] = keys[i];
     packed[i] = pos;  // keep the staging slot for the payload
   }
+  if constexpr (kVals) {
+    // The payload source may be the staging buffer itself: read every
+    // thread's payloads before any is overwritten.
+    uint32_t v[ITEMS];
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+      const int p = wpos + i * kWarp;
+      v[i] = io.val_src == nullptr ? static_cast<uint32_t>(tile_begin + p)
+                                   : ((FULL || p < valid) ? io.val_src[p] : 0u);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) io.stage_vals[packed[i]] = v[i];
+  }
+  LSDRS_PHASE(3);  // staging (thread 0's share)
 
   // ---- 6. decoupled look-back -------------------------------------------
   if (tid < R) {
     uint32_t excl = 0;
     if (t > 0) {
-      excl = look_back<R>(a.status + (tile - t) * R + tid, t, a.error, a.timeout_ns, trips, polls);
+      excl = look_back<R, WIN>(a.status + (tile - t) * R + tid, t, a.error, a.timeout_ns, trips, polls);
       st_relaxed(status_tile + tid, kFlagP | (excl + my_count));
     }
     s.g_off[tid] = a.bases[row * a.bases_row_stride + tid] + excl - s.tile_start[tid];
   }
+  LSDRS_PHASE(4);  // thread 0's look-back
 #if LSDRS_STATS
   if (trips) atomicAdd(a.error + kStatsWord, trips);
   if (polls) atomicAdd(a.error + kStatsWord + 1, polls);
 #endif
   __syncthreads();
+  LSDRS_PHASE(5);  // wait for the slowest digit's look-back
 
   // ---- 7. contiguous per-digit runs out ---------------------------------
   T* kout = static_cast<T*>(a.keys_out) + row_base;
-  uint32_t dst[kVals ? ITEMS : 1];
+  uint32_t* vout32 = static_cast<uint32_t*>(a.vals_out) + row_base;
+  int64_t* vout64 = static_cast<int64_t*>(a.vals_out) + row_base;
+  const bool wide = VK == kValIdx && a.wide_out;
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
     const int j = i * THREADS + tid;
     if (FULL || j < valid) {
-      const T k = stage_keys[j];
+      const T k = io.stage_keys[j];
       const uint32_t d = KeyOp::digit(k, a.shift, a.mask, a.flip);
       const uint32_t g = s.g_off[d] + static_cast<uint32_t>(j);
       kout[g] = k;
-      if constexpr (kVals) dst[i] = g;
-    }
-  }
-  if constexpr (kVals) {
-    if (vals_tma && !mbar_wait_bounded(&s.bar, 0, a.timeout_ns)) {
-      atomicCAS(a.error, kErrNone, kErrLookback);
-      mbar_wait_bounded(&s.bar, 0, a.timeout_ns);  // let the copy land before leaving
-      return;
-    }
-    __syncthreads();  // staged keys consumed; payloads visible
-#pragma unroll
-    for (int i = 0; i < ITEMS; ++i) {
-      const uint32_t v = gen_idx ? static_cast<uint32_t>(tile_begin + wpos + i * kWarp)
-                                 : s.vin[wpos + i * kWarp];
-      stage_vals[packed[i]] = v;
-    }
-    __syncthreads();
-    if (VK == kValIdx && a.wide_out) {
-      int64_t* vout = static_cast<int64_t*>(a.vals_out) + row_base;
-#pragma unroll
-      for (int i = 0; i < ITEMS; ++i) {
-        const int j = i * THREADS + tid;
-        if (FULL || j < valid)
-          vout[dst[i]] = static_cast<int64_t>(static_cast<int32_t>(stage_vals[j]));
-      }
-    } else {
-      uint32_t* vout = static_cast<uint32_t*>(a.vals_out) + row_base;
-#pragma unroll
-      for (int i = 0; i < ITEMS; ++i) {
-        const int j = i * THREADS + tid;
-        if (FULL || j < valid) vout[dst[i]] = stage_vals[j];
+      if constexpr (kVals) {
+        const uint32_t v = io.stage_vals[j];
+        if (wide)
+          vout64[g] = static_cast<int64_t>(static_cast<int32_t>(v));
+        else
+          vout32[g] = v;
       }
     }
   }
+  LSDRS_PHASE(6);  // write-out
 }
 
-template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB>
-__global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
-  using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
-  constexpr int R = S::kRadix;
-  constexpr int W = S::kWarps;
+// ------------------------------------------------------------------------
+// Persistent form: each CTA loops over tiles taken from the counter and,
+// while it works on one tile, has the next tile's keys and payloads already
+// streaming into its second shared-memory slot by bulk (TMA) copies.  The
+// slot being processed doubles as the staging buffer.  Tiles that cannot be
+// copied in bulk (the ragged last tile of a row, or buffers not 16-byte
+// aligned) are read with ordinary loads instead.
+// ------------------------------------------------------------------------
+template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS>
+struct PersistentSmem {
+  using T = typename KeyOp::T;
+  static constexpr int kTile = THREADS * ITEMS;
+  static constexpr bool kVals = VK != kValNone;
+  struct Slot {
+    alignas(128) T keys[kTile];
+    alignas(128) uint32_t vals[kVals ? kTile : 4];
+  };
+  Slot slot[2];
+  TileScratch<THREADS / kWarp, (1 << BITS)> scratch;
+  uint64_t bar[2];
+  uint32_t next_tile;
+  uint32_t abort;
+};
+
+struct TilePlace {
+  int64_t row, t, tile_begin;
+  int valid;
+  bool bulk;  // full tile whose sources are 16-byte aligned
+};
+
+template <class KeyOp, int VK, int TILE>
+__device__ __forceinline__ TilePlace place_tile(const SweepArgs& a, int64_t tile) {
+  TilePlace p;
+  p.row = tile / a.tiles_per_row;
+  p.t = tile - p.row * a.tiles_per_row;
+  p.tile_begin = p.t * TILE;
+  p.valid = static_cast<int>(a.cols - p.tile_begin < TILE ? a.cols - p.tile_begin : TILE);
+  const int64_t off = p.row * a.cols + p.tile_begin;
+  const auto* k = static_cast<const typename KeyOp::T*>(a.keys_in) + off;
+  bool ok = p.valid == TILE && (reinterpret_cast<uintptr_t>(k) & 15) == 0;
+  if (VK != kValNone && a.vals_in != nullptr)
+    ok = ok && (reinterpret_cast<uintptr_t>(static_cast<const uint32_t*>(a.vals_in) + off) & 15) == 0;
+  p.bulk = ok;
+  return p;
+}
+
+template <class KeyOp, int VK, int TILE, class Slot>
+__device__ __forceinline__ void issue_tile_copy(const SweepArgs& a, const TilePlace& p, Slot& slot,
+                                                uint64_t* bar) {
+  using T = typename KeyOp::T;
+  const int64_t off = p.row * a.cols + p.tile_begin;
+  const bool vals = VK != kValNone && a.vals_in != nullptr;
+  const uint32_t bytes = TILE * sizeof(T) + (vals ? TILE * sizeof(uint32_t) : 0u);
+  mbar_arrive_expect_tx(bar, bytes);
+  bulk_copy_g2s(slot.keys, static_cast<const T*>(a.keys_in) + off, TILE * sizeof(T), bar);
+  if (vals)
+    bulk_copy_g2s(slot.vals, static_cast<const uint32_t*>(a.vals_in) + off,
+                  TILE * sizeof(uint32_t), bar);
+}
+
+template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB, int WIN>
+__global__ void __launch_bounds__(THREADS, MINB) onesweep_persistent_kernel(SweepArgs a,
+                                                                            uint32_t ntiles) {
+  using S = PersistentSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
+  using T = typename KeyOp::T;
+  constexpr int R = 1 << BITS;
+  constexpr int W = THREADS / kWarp;
   constexpr int TILE = S::kTile;
   static_assert(R <= THREADS, "one thread per digit");
   static_assert(kWarp * ITEMS < 65536, "ranks are packed in 16 bits");
 
-  extern __shared__ __align__(16) unsigned char smem_raw[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  S& s = *reinterpret_cast<S*>(smem_raw);
+  const int tid = threadIdx.x;
+
+  if (tid == 0) {
+    mbar_init(&s.bar[0], 1);
+    mbar_init(&s.bar[1], 1);
+    const uint32_t t0 = atomicAdd(a.tile_counter, 1u);
+    s.next_tile = t0;
+    if (t0 < ntiles) {
+      const TilePlace p = place_tile<KeyOp, VK, TILE>(a, t0);
+      if (p.bulk) issue_tile_copy<KeyOp, VK, TILE>(a, p, s.slot[0], &s.bar[0]);
+    }
+  }
+  __syncthreads();
+  uint32_t tile = s.next_tile;
+  uint32_t parity[2] = {0u, 0u};
+  int cur = 0;
+  while (tile < ntiles) {
+    // Everyone is done with the other slot (previous tile): order those
+    // generic-proxy accesses before the bulk copy that refills it.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (tid == 0) {
+      const uint32_t nt = atomicAdd(a.tile_counter, 1u);
+      s.next_tile = nt;
+      s.abort = ld_relaxed(a.error) != kErrNone;
+      if (nt < ntiles) {
+        const TilePlace pn = place_tile<KeyOp, VK, TILE>(a, nt);
+        if (pn.bulk) issue_tile_copy<KeyOp, VK, TILE>(a, pn, s.slot[cur ^ 1], &s.bar[cur ^ 1]);
+      }
+    }
+    for (int i = tid; i < W * R; i += THREADS) (&s.scratch.warp_cnt[0][0])[i] = 0;
+    const TilePlace p = place_tile<KeyOp, VK, TILE>(a, tile);
+    bool ready = true;
+    if (p.bulk) {
+      ready = mbar_wait_bounded(&s.bar[cur], parity[cur], a.timeout_ns);
+      parity[cur] ^= 1u;
+    }
+    __syncthreads();
+    const uint32_t next = s.next_tile;
+    if (!ready) atomicCAS(a.error, kErrNone, kErrLookback);
+    if (s.abort || !ready) {
+      if (tid < R) st_relaxed(a.status + static_cast<int64_t>(tile) * R + tid, kFlagP);
+    } else {
+      const int64_t off = p.row * a.cols + p.tile_begin;
+      TileIo<KeyOp> io;
+      io.stage_keys = s.slot[cur].keys;
+      io.stage_vals = s.slot[cur].vals;
+      io.key_src = p.bulk ? s.slot[cur].keys : static_cast<const T*>(a.keys_in) + off;
+      io.val_src = nullptr;
+      if (VK != kValNone && a.vals_in != nullptr)
+        io.val_src = p.bulk ? s.slot[cur].vals : static_cast<const uint32_t*>(a.vals_in) + off;
+      if (p.valid == TILE)
+        sweep_tile<true, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io, tile, p.row, p.t, p.valid);
+      else
+        sweep_tile<false, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io, tile, p.row, p.t, p.valid);
+    }
+    if (a.status_zero != nullptr && tid < R) a.status_zero[static_cast<int64_t>(tile) * R + tid] = 0;
+    tile = next;
+    cur ^= 1;
+  }
+}
+
+// ------------------------------------------------------------------------
+// One-tile-per-CTA form: the grid has one CTA per tile; payloads of full,
+// aligned tiles come by one bulk copy into a separate buffer.
+// ------------------------------------------------------------------------
+template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS>
+struct SweepSmem {
+  using T = typename KeyOp::T;
+  static constexpr int kTile = THREADS * ITEMS;
+  static constexpr bool kVals = VK != kValNone;
+  alignas(128) T keys[kTile];                      // key stage
+  alignas(128) uint32_t vals[kVals ? kTile : 4];   // payloads in, then payload stage
+  TileScratch<THREADS / kWarp, (1 << BITS)> scratch;
+  uint64_t bar;
+  uint32_t tile_id;
+  uint32_t abort;
+};
+
+template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB, int WIN>
+__global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
+  using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
+  using T = typename KeyOp::T;
+  constexpr int R = 1 << BITS;
+  constexpr int W = THREADS / kWarp;
+  constexpr int TILE = S::kTile;
+  static_assert(R <= THREADS, "one thread per digit");
+  static_assert(kWarp * ITEMS < 65536, "ranks are packed in 16 bits");
+
+  extern __shared__ __align__(128) unsigned char smem_raw[];
   S& s = *reinterpret_cast<S*>(smem_raw);
   const int tid = threadIdx.x;
 
@@ -388,50 +533,91 @@ __global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
     s.tile_id = atomicAdd(a.tile_counter, 1u);
     s.abort = ld_relaxed(a.error) != kErrNone;
   }
-  for (int i = tid; i < W * R; i += THREADS) (&s.warp_cnt[0][0])[i] = 0;
+  for (int i = tid; i < W * R; i += THREADS) (&s.scratch.warp_cnt[0][0])[i] = 0;
   __syncthreads();
 
   const int64_t tile = s.tile_id;
-  const int64_t row = tile / a.tiles_per_row;
-  const int64_t t = tile - row * a.tiles_per_row;
-  const int64_t tile_begin = t * TILE;
-  const int valid = static_cast<int>(a.cols - tile_begin < TILE ? a.cols - tile_begin : TILE);
-
-  if (s.abort) {  // an earlier tile failed: release successors and stop
+  const TilePlace p = place_tile<KeyOp, VK, TILE>(a, tile);
+  const int64_t off = p.row * a.cols + p.tile_begin;
+  bool ready = true;
+  TileIo<KeyOp> io;
+  io.key_src = static_cast<const T*>(a.keys_in) + off;
+  io.stage_keys = s.keys;
+  io.stage_vals = s.vals;
+  io.val_src = nullptr;
+  if (VK != kValNone && a.vals_in != nullptr) {
+    const uint32_t* vsrc = static_cast<const uint32_t*>(a.vals_in) + off;
+    io.val_src = vsrc;
+    if (p.bulk && LSDRS_VALS_TMA) {
+      if (tid == 0) {
+        mbar_init(&s.bar, 1);
+        mbar_arrive_expect_tx(&s.bar, TILE * sizeof(uint32_t));
+        bulk_copy_g2s(s.vals, vsrc, TILE * sizeof(uint32_t), &s.bar);
+      }
+      __syncthreads();
+      ready = mbar_wait_bounded(&s.bar, 0, a.timeout_ns);
+      io.val_src = s.vals;
+    }
+  }
+  if (!ready) atomicCAS(a.error, kErrNone, kErrLookback);
+  if (s.abort || !ready) {  // an earlier tile failed: release successors and stop
     if (tid < R) st_relaxed(a.status + tile * R + tid, kFlagP);
-  } else if (valid == TILE) {
-    sweep_tile<true>(a, s, tile, row, t, valid);
+  } else if (p.valid == TILE) {
+    sweep_tile<true, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io, tile, p.row, p.t, p.valid);
   } else {
-    sweep_tile<false>(a, s, tile, row, t, valid);
+    sweep_tile<false, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io, tile, p.row, p.t, p.valid);
   }
   if (a.status_zero != nullptr && tid < R) a.status_zero[tile * R + tid] = 0;
 }
 
-template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB>
+#ifndef LSDRS_PERSISTENT
+#define LSDRS_PERSISTENT 0
+#endif
+
+template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB, int WIN>
 cudaError_t launch_sweep_t(const SweepArgs& a, int64_t grid, cudaStream_t s) {
+#if LSDRS_PERSISTENT
+  using S = PersistentSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
+  auto kern = onesweep_persistent_kernel<KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>;
+#else
   using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
-  auto kern = onesweep_kernel<KeyOp, BITS, VK, THREADS, ITEMS, MINB>;
+  auto kern = onesweep_kernel<KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>;
+#endif
   const size_t smem = sizeof(S);
   if (smem > 48 * 1024) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
+#if LSDRS_PERSISTENT
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, THREADS, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int64_t ctas = static_cast<int64_t>(sms) * per_sm < grid
+                           ? static_cast<int64_t>(sms) * per_sm
+                           : grid;
+  kern<<<static_cast<unsigned>(ctas), THREADS, smem, s>>>(a, static_cast<uint32_t>(grid));
+#else
   kern<<<static_cast<unsigned>(grid), THREADS, smem, s>>>(a);
+#endif
   return cudaGetLastError();
 }
 
-template <class KeyOp, int VK, int THREADS, int ITEMS, int MINB>
+template <class KeyOp, int VK, int THREADS, int ITEMS, int MINB, int WIN>
 cudaError_t launch_sweep_bits(int bits, const SweepArgs& a, int64_t grid, cudaStream_t s) {
   switch (bits) {
-    case 1: return launch_sweep_t<KeyOp, 1, VK, THREADS, ITEMS, MINB>(a, grid, s);
-    case 2: return launch_sweep_t<KeyOp, 2, VK, THREADS, ITEMS, MINB>(a, grid, s);
-    case 3: return launch_sweep_t<KeyOp, 3, VK, THREADS, ITEMS, MINB>(a, grid, s);
-    case 4: return launch_sweep_t<KeyOp, 4, VK, THREADS, ITEMS, MINB>(a, grid, s);
-    case 5: return launch_sweep_t<KeyOp, 5, VK, THREADS, ITEMS, MINB>(a, grid, s);
-    case 6: return launch_sweep_t<KeyOp, 6, VK, THREADS, ITEMS, MINB>(a, grid, s);
-    case 7: return launch_sweep_t<KeyOp, 7, VK, THREADS, ITEMS, MINB>(a, grid, s);
-    case 8: return launch_sweep_t<KeyOp, 8, VK, THREADS, ITEMS, MINB>(a, grid, s);
+    case 1: return launch_sweep_t<KeyOp, 1, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
+    case 2: return launch_sweep_t<KeyOp, 2, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
+    case 3: return launch_sweep_t<KeyOp, 3, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
+    case 4: return launch_sweep_t<KeyOp, 4, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
+    case 5: return launch_sweep_t<KeyOp, 5, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
+    case 6: return launch_sweep_t<KeyOp, 6, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
+    case 7: return launch_sweep_t<KeyOp, 7, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
+    case 8: return launch_sweep_t<KeyOp, 8, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
