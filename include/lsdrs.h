@@ -57,8 +57,9 @@ typedef enum rs_status {
 
 typedef enum rs_float_kind { RS_F16 = 0, RS_BF16 = 1 } rs_float_kind;
 
-/* Largest number of keys in one sort (or one row of a row-wise sort): the
- * look-back words hold 30-bit counts. */
+/* Largest number of keys in one sort (or one row of a row-wise sort); the
+ * device offsets are 32-bit and the bound matches the row limit of the
+ * row-wise sort (FlagTree PR #1084: n < 2^30). */
 #define RS_MAX_KEYS ((size_t)((1u << 30) - 1u))
 
 /* Size in bytes of the scratch buffer a flat sort needs.
