@@ -53,16 +53,13 @@ cudaError_t timed_launch(int kernel, uint64_t units, cudaStream_t s, F&& launch)
 // -------------------------------------------------------------------- plan
 // Scratch layout (offsets in bytes from `temp`, each 256-byte aligned):
 //   header   : word 0 = device error word, words 1..64 = tile counters
-//   flags    : look-back tile flags, [passes][tiles] u32
-//   counts   : look-back tile digit counts, [tiles][radix] u32
-//   incl     : look-back inclusive digit prefixes, [tiles][radix] u32
+//   status0  : look-back words of even passes  [tiles][radix] u32
+//   status1  : look-back words of odd passes   [tiles][radix] u32
 //   bases    : [rows][passes][radix] u32
 //   slots    : [rows][hist chunks][passes][radix] u32 partial histograms
 //   alt_keys : ping-pong key buffer
 //   alt_vals : ping-pong payload buffer (u32 / int32 indices)
-// header and flags are contiguous: K-HIST zeroes them in one range.  counts
-// and incl are reused by every pass; a tile's words are only read after its
-// flag for the current pass says they were written.
+// header and status0 are contiguous: K-HIST zeroes them in one range.
 constexpr size_t kHeaderBytes = 512;
 constexpr int kMaxPasses = 64;
 
@@ -77,7 +74,7 @@ struct Plan {
   int64_t tiles_per_row, tiles;
   int chunks_per_row;
   int64_t chunk_len;
-  size_t off_flags, off_counts, off_incl, off_bases, off_slots, off_alt_keys, off_alt_vals, total;
+  size_t off_status0, off_status1, off_bases, off_slots, off_alt_keys, off_alt_vals, total;
 };
 
 rs_status make_plan(KeyKind key, ValKind val, int64_t rows, int64_t cols, int begin_bit,
@@ -113,15 +110,13 @@ rs_status make_plan(KeyKind key, ValKind val, int64_t rows, int64_t cols, int be
   p.chunk_len = (cols + want - 1) / want;
   p.chunk_len = static_cast<int64_t>(align_up(static_cast<size_t>(p.chunk_len), 64));
 
-  const size_t words_bytes = align_up(static_cast<size_t>(p.tiles) * p.radix * 4, 256);
+  const size_t status_bytes = align_up(static_cast<size_t>(p.tiles) * p.radix * 4, 256);
   const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols);
   size_t off = kHeaderBytes;
-  p.off_flags = off;
-  off += align_up(static_cast<size_t>(p.tiles) * p.passes * 4, 256);
-  p.off_counts = off;
-  off += words_bytes;
-  p.off_incl = off;
-  off += words_bytes;
+  p.off_status0 = off;
+  off += status_bytes;
+  p.off_status1 = off;
+  off += status_bytes;
   p.off_bases = off;
   off += align_up(static_cast<size_t>(rows) * p.passes * p.radix * 4, 256);
   p.off_slots = off;
@@ -157,7 +152,7 @@ rs_status run_front(const Plan& p, const void* keys, uint32_t flip, void* temp,
   h.flip = flip;
   h.slots = reinterpret_cast<uint32_t*>(at(temp, p.off_slots));
   h.zero_ptr = reinterpret_cast<uint32_t*>(temp);
-  h.zero_words = p.off_counts / 4;  // header + flags of every pass
+  h.zero_words = (p.off_status1) / 4;  // header + status0
   const int64_t hgrid = p.rows * p.chunks_per_row;
   const uint64_t n = static_cast<uint64_t>(p.rows) * p.cols;
   cudaError_t e = timed_launch(0, n, s, [&] {
@@ -229,9 +224,8 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
   if (st != RS_OK) return st;
 
   uint32_t* header = reinterpret_cast<uint32_t*>(temp);
-  uint32_t* flags = reinterpret_cast<uint32_t*>(at(temp, p.off_flags));
-  uint32_t* counts = reinterpret_cast<uint32_t*>(at(temp, p.off_counts));
-  uint32_t* incl = reinterpret_cast<uint32_t*>(at(temp, p.off_incl));
+  uint32_t* status[2] = {reinterpret_cast<uint32_t*>(at(temp, p.off_status0)),
+                         reinterpret_cast<uint32_t*>(at(temp, p.off_status1))};
   void* alt_keys = at(temp, p.off_alt_keys);
   void* alt_vals = at(temp, p.off_alt_vals);
   const uint32_t* bases = reinterpret_cast<const uint32_t*>(at(temp, p.off_bases));
@@ -261,9 +255,8 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
     a.flip = flip;
     a.bases = bases + static_cast<size_t>(q) * p.radix;
     a.bases_row_stride = static_cast<int64_t>(p.passes) * p.radix;
-    a.flags = flags + static_cast<size_t>(q) * p.tiles;
-    a.counts = counts;
-    a.incl = incl;
+    a.status = status[q & 1];
+    a.status_zero = last ? nullptr : status[(q + 1) & 1];
     a.tile_counter = header + 1 + q;
     a.error = header;
     a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);

@@ -11,11 +11,13 @@ namespace lsdrs {
 constexpr int kWarp = 32;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
-// Look-back tile flags: 0 = nothing published yet, A = the tile's digit
-// counts are published, P = its inclusive digit prefixes (over the row's
-// tiles up to and including it) are published.
-constexpr uint32_t kTileA = 1u;
-constexpr uint32_t kTileP = 2u;
+// Look-back status word: [P:1][A:1][value:30].  A = the tile's own digit
+// count is published; P = the inclusive prefix over the row's tiles up to
+// this one is published.  Zero means "nothing yet".
+constexpr uint32_t kFlagA = 1u << 30;
+constexpr uint32_t kFlagP = 1u << 31;
+constexpr uint32_t kValueMask = kFlagA - 1u;
+constexpr uint64_t kMaxRowLen = kValueMask;  // counts must fit in 30 bits
 
 // Device error word values (mirrors rs_status).
 constexpr uint32_t kErrNone = 0;
@@ -49,18 +51,6 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
 
 __device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Acquire/release accesses for the tile flags that gate the count and
-// prefix words written before them.
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Streaming loads of data read exactly once per pass.

@@ -19,42 +19,58 @@ struct SweepShape {
   int threads;
   int items;
   int min_blocks;  // resident CTAs per SM the register budget is sized for
+  int window;      // look-back words read per round trip
   constexpr int tile() const { return threads * items; }
 };
 // Shapes may be overridden at build time for tuning sweeps, e.g.
-// -DLSDRS_U32P_T=256 -DLSDRS_U32P_I=16 -DLSDRS_U32P_B=4 (threads, items per
-// thread, CTAs per SM); the defaults
+// -DLSDRS_U32P_T=256 -DLSDRS_U32P_I=16 -DLSDRS_U32P_B=4 -DLSDRS_U32P_W=4
+// (threads, items per thread, CTAs per SM, look-back window); the defaults
 // are the fastest measured on GB300 for 2^28-key sorts.
 #ifndef LSDRS_U32K_T
 #define LSDRS_U32K_T 256
 #define LSDRS_U32K_I 24
 #define LSDRS_U32K_B 4
 #endif
+#ifndef LSDRS_U32K_W
+#define LSDRS_U32K_W 8
+#endif
 #ifndef LSDRS_U32P_T
 #define LSDRS_U32P_T 256
 #define LSDRS_U32P_I 16
 #define LSDRS_U32P_B 4
+#endif
+#ifndef LSDRS_U32P_W
+#define LSDRS_U32P_W 4
 #endif
 #ifndef LSDRS_U64K_T
 #define LSDRS_U64K_T 256
 #define LSDRS_U64K_I 12
 #define LSDRS_U64K_B 4
 #endif
+#ifndef LSDRS_U64K_W
+#define LSDRS_U64K_W 4
+#endif
 #ifndef LSDRS_U64P_T
 #define LSDRS_U64P_T 256
 #define LSDRS_U64P_I 12
 #define LSDRS_U64P_B 4
+#endif
+#ifndef LSDRS_U64P_W
+#define LSDRS_U64P_W 4
 #endif
 #ifndef LSDRS_F16_T
 #define LSDRS_F16_T 256
 #define LSDRS_F16_I 16
 #define LSDRS_F16_B 4
 #endif
-constexpr SweepShape kShapeU32Keys{LSDRS_U32K_T, LSDRS_U32K_I, LSDRS_U32K_B};
-constexpr SweepShape kShapeU32Pairs{LSDRS_U32P_T, LSDRS_U32P_I, LSDRS_U32P_B};
-constexpr SweepShape kShapeU64Keys{LSDRS_U64K_T, LSDRS_U64K_I, LSDRS_U64K_B};
-constexpr SweepShape kShapeU64Pairs{LSDRS_U64P_T, LSDRS_U64P_I, LSDRS_U64P_B};
-constexpr SweepShape kShapeF16Idx{LSDRS_F16_T, LSDRS_F16_I, LSDRS_F16_B};
+#ifndef LSDRS_F16_W
+#define LSDRS_F16_W 4
+#endif
+constexpr SweepShape kShapeU32Keys{LSDRS_U32K_T, LSDRS_U32K_I, LSDRS_U32K_B, LSDRS_U32K_W};
+constexpr SweepShape kShapeU32Pairs{LSDRS_U32P_T, LSDRS_U32P_I, LSDRS_U32P_B, LSDRS_U32P_W};
+constexpr SweepShape kShapeU64Keys{LSDRS_U64K_T, LSDRS_U64K_I, LSDRS_U64K_B, LSDRS_U64K_W};
+constexpr SweepShape kShapeU64Pairs{LSDRS_U64P_T, LSDRS_U64P_I, LSDRS_U64P_B, LSDRS_U64P_W};
+constexpr SweepShape kShapeF16Idx{LSDRS_F16_T, LSDRS_F16_I, LSDRS_F16_B, LSDRS_F16_W};
 constexpr SweepShape sweep_shape(KeyKind k, ValKind v) {
   return k == kKeyU32 ? (v == kValNone ? kShapeU32Keys : kShapeU32Pairs)
        : k == kKeyU64 ? (v == kValNone ? kShapeU64Keys : kShapeU64Pairs)
@@ -102,9 +118,8 @@ struct SweepArgs {
   int wide_out;            // kValIdx: write int64 indices
   const uint32_t* bases;   // bases of this pass for row 0
   int64_t bases_row_stride;
-  uint32_t* flags;         // [rows * tiles_per_row] this pass's tile flags (zeroed)
-  uint32_t* counts;        // [rows * tiles_per_row][radix] tile digit counts
-  uint32_t* incl;          // [rows * tiles_per_row][radix] inclusive prefixes
+  uint32_t* status;        // [rows * tiles_per_row][radix] look-back words
+  uint32_t* status_zero;   // next pass's look-back words, zeroed here
   uint32_t* tile_counter;
   uint32_t* error;
   uint64_t timeout_ns;

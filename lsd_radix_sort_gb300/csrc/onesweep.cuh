@@ -11,33 +11,32 @@
 //     order and every tile a CTA waits on belongs to a CTA that is already
 //     running (forward progress of the look-back).
 //  2. The tile's payloads are requested at once with one bulk (TMA) copy into
-//     shared memory; they are not needed before step 5.  Keys are loaded
+//     shared memory; they are not needed before step 7.  Keys are loaded
 //     warp-striped into registers: warp w owns a contiguous run of 32*ITEMS
 //     keys and its item i covers keys 32*i .. 32*i+31 of that run, one per
 //     lane, so (warp, item, lane) order is input order.
 //  3. Rank within the warp: for each item, the lanes holding the same digit
-//     are found (one ballot per digit bit, or a shared-memory bit mask per
-//     digit that the lanes OR themselves into); a lane's rank is the number
-//     of such peers in lower lanes plus the warp's running count of that
-//     digit (a per-warp shared-memory counter that the lowest peer
-//     advances).  This is the per-digit exclusive scan of the indicator
-//     "digit == d" (section 13.2's rank within digit) for all digits at once.
+//     are found by one ballot per digit bit; a lane's rank is the number of
+//     such peers in lower lanes plus the warp's running count of that digit
+//     (a per-warp shared-memory counter that the lowest peer advances).
+//     This is the per-digit exclusive scan of the indicator "digit == d"
+//     (section 13.2's rank within digit), done for all digits at once.
 //  4. A per-digit scan over the warps gives each warp's offset and the
-//     tile's digit counts, which are published at once for later tiles
-//     (decoupled look-back: counts, then flag A); a scan over the digits
-//     gives each digit's start inside the tile.
-//  5. Keys, then payloads, are placed in shared memory in tile-sorted order.
-//     Meanwhile one warp looks back over the predecessors' flags, 32 tiles
-//     per round trip, for the nearest tile whose inclusive prefixes are out
-//     (flag P); each digit then adds that tile's prefix and the counts of
-//     the tiles in between, and this tile publishes its own prefixes and P.
-//     The precomputed alternative (per-tile offsets from a separate pass,
-//     FlagTree PR #1084 section 2) needs a second read of the keys; the
-//     look-back needs none.  Every wait is bounded in time.
-//  6. Thread j writes staged key j (and its payload) to
-//     base[d] + prefix[d] + (j - start[d]): every digit's keys leave as one
-//     contiguous run ("100 Days of GPU", day 35: after the local sort the
-//     write out is one run per digit).
+//     tile's digit counts; the counts are published at once for later tiles
+//     (decoupled look-back, flag A), then a scan over the digits gives each
+//     digit's start inside the tile.
+//  5. Keys are placed in shared memory in tile-sorted order.
+//  6. Look-back: for each digit, the counts of earlier tiles of the row are
+//     summed walking backwards, a window of tiles per memory round trip,
+//     until a tile that has published its inclusive prefix (flag P); this
+//     tile then publishes its own inclusive prefix.  The precomputed
+//     alternative (per-tile offsets from a separate pass, FlagTree PR #1084
+//     section 2) needs a second read of the keys; the look-back needs none.
+//     Every wait is bounded in time.
+//  7. Thread j writes staged key j to base[d] + prefix[d] + (j - start[d]):
+//     every digit's keys leave as one contiguous run ("100 Days of GPU",
+//     day 35: after the local sort the write out is one run per digit).
+//     Payloads follow through the same staging buffer.
 // Lanes past the end of the last tile take the highest digit, rank after
 // every real key of the tile, are not counted in the published counts and
 // are not stored (the page's sentinel padding, without the padding).  Full
@@ -47,11 +46,15 @@
 #include "kernels.h"
 #include "keys.cuh"
 
-// Build-time options: the warp ranking method (0 = per-bit ballots,
-// 1 = hardware match, 2 = shared-memory bit masks), the bulk copy of
-// payloads, and look-back statistics / phase timers for measurement builds.
-#ifndef LSDRS_RANK
-#define LSDRS_RANK 0
+// Tuning knobs (build-time): a sleep between polls of a word that is not
+// ready, the hardware
+// match instruction instead of per-bit ballots, the bulk copy of payloads,
+// and look-back statistics for measurement builds.
+#ifndef LSDRS_SPIN_SLEEP_NS
+#define LSDRS_SPIN_SLEEP_NS 0
+#endif
+#ifndef LSDRS_MATCH_ANY
+#define LSDRS_MATCH_ANY 0
 #endif
 #ifndef LSDRS_VALS_TMA
 #define LSDRS_VALS_TMA 1
@@ -63,9 +66,9 @@
 namespace lsdrs {
 
 // Header words of the scratch buffer that measurement builds accumulate
-// look-back statistics into (flag round trips, polls of unready flags), and,
-// with LSDRS_STATS >= 2, per-phase cycle sums of thread 0 as 64-bit counters
-// from word kPhaseWord on.
+// look-back statistics into (look-back round trips, polls of unready words),
+// and, with LSDRS_STATS >= 2, per-phase cycle sums of thread 0 as 64-bit
+// counters from word kPhaseWord on.
 constexpr int kStatsWord = 100;
 constexpr int kPhaseWord = 104;
 #if LSDRS_STATS >= 2
@@ -84,10 +87,10 @@ constexpr int kPhaseWord = 104;
   } while (0)
 #endif
 
-// Lanes of the warp whose digit equals this lane's digit, by votes.
+// Lanes of the warp whose digit equals this lane's digit.
 template <int BITS>
 __device__ __forceinline__ uint32_t digit_peers(uint32_t d) {
-#if LSDRS_RANK == 1
+#if LSDRS_MATCH_ANY
   return __match_any_sync(kFull, d);
 #else
   uint32_t peers = kFull;
@@ -102,53 +105,78 @@ __device__ __forceinline__ uint32_t digit_peers(uint32_t d) {
 #endif
 }
 
-// Run by one whole warp: the nearest predecessor within the row whose flag
-// is P, found 32 flags per round trip.  Returns that tile's index in the
-// row, or -1 when the wait gave up (timeout, or an error reported
-// elsewhere); then *stop is the tile it gave up on, and only the counts
-// after it are summed, which underestimates every prefix and keeps every
-// store in bounds.  Otherwise *stop equals the returned index.
-__device__ __forceinline__ int64_t find_inclusive(const uint32_t* row_flags, int64_t t,
-                                                  uint32_t* error, uint64_t timeout_ns,
-                                                  int64_t* stop, uint32_t& trips,
-                                                  uint32_t& polls) {
-  const uint32_t lane = threadIdx.x & 31;
-  int64_t base = t - 1;  // newest tile not yet known to hold counts
-  uint64_t t0 = 0;
+// Bounded wait for a non-zero look-back word.  On timeout, or when another
+// tile has already reported an error, records the error and returns a word
+// with flag P and value 0 so that the walk ends.
+__device__ __forceinline__ uint32_t wait_status(const uint32_t* p, uint32_t* error,
+                                                uint64_t timeout_ns, uint32_t& polls) {
+  uint32_t v = ld_relaxed(p);
+  if (v != 0) return v;
+  const uint64_t t0 = global_timer_ns();
   uint32_t spins = 0;
   for (;;) {
-    const int64_t k = base - static_cast<int64_t>(lane);
-    const uint32_t f = k >= 0 ? ld_acquire(row_flags + k) : kTileP;
-    const uint32_t pm = __ballot_sync(kFull, f == kTileP);
-    const uint32_t zm = __ballot_sync(kFull, f == 0u);
+#if LSDRS_SPIN_SLEEP_NS > 0
+    __nanosleep(LSDRS_SPIN_SLEEP_NS);
+#endif
+    v = ld_relaxed(p);
+    ++spins;
+    if (v != 0) break;
+    if ((spins & 63u) == 0) {
+      if (ld_relaxed(error) != kErrNone) {
+        v = kFlagP;
+        break;
+      }
+      if (global_timer_ns() - t0 > timeout_ns) {
+        atomicCAS(error, kErrNone, kErrLookback);
+        v = kFlagP;
+        break;
+      }
+    }
+  }
+  polls += spins;
+  return v;
+}
+
+// Exclusive prefix of one digit over tiles [0, t) of a row.  `col` points at
+// this digit's word of the row's tile 0; tile k's word is col[k * R].  Each
+// round trip loads the words of WIN predecessors at once (for the 32 digits
+// of a warp these are coalesced 128-byte rows) and consumes them up to the
+// first inclusive prefix, or up to the first word not yet published, on
+// which it then waits.
+template <int R, int WIN>
+__device__ __forceinline__ uint32_t look_back(const uint32_t* col, int64_t t, uint32_t* error,
+                                              uint64_t timeout_ns, uint32_t& trips,
+                                              uint32_t& polls) {
+  static_assert(WIN >= 1 && WIN <= 32, "window of 1..32 tiles");
+  uint32_t excl = 0;
+  int64_t pt = t - 1;  // newest predecessor not yet consumed
+  for (;;) {
+    uint32_t v[WIN];
+#pragma unroll
+    for (int k = 0; k < WIN; ++k) v[k] = (pt - k >= 0) ? ld_relaxed(col + (pt - k) * R) : kFlagP;
     ++trips;
-    const int fp = pm ? __ffs(pm) - 1 : 32;
-    const int fz = zm ? __ffs(zm) - 1 : 32;
-    if (fp < fz) {
-      *stop = base - fp;
-      return base - fp;
+    uint32_t zero_mask = 0, p_mask = 0;
+#pragma unroll
+    for (int k = 0; k < WIN; ++k) {
+      zero_mask |= (v[k] == 0 ? 1u : 0u) << k;
+      p_mask |= (v[k] >> 31) << k;
     }
-    if (fz == 32) {
-      base -= 32;
-      continue;
-    }
-    // tile base - fz has not published its counts yet: wait for it
-    base -= fz;
-    ++polls;
-    if (spins == 0) t0 = global_timer_ns();
-    if ((++spins & 63u) == 0) {
-      uint32_t give_up = 0;
-      if (lane == 0) {
-        give_up = ld_relaxed(error) != kErrNone;
-        if (!give_up && global_timer_ns() - t0 > timeout_ns) {
-          atomicCAS(error, kErrNone, kErrLookback);
-          give_up = 1;
-        }
-      }
-      if (__shfl_sync(kFull, give_up, 0)) {
-        *stop = base;
-        return -1;
-      }
+    // consume words [0, stop): up to and including the first P, or up to
+    // (not including) the first unpublished word, whichever comes first.
+    const int first_p = p_mask ? __ffs(p_mask) - 1 : WIN;
+    const int first_zero = zero_mask ? __ffs(zero_mask) - 1 : WIN;
+    const bool done = first_p < first_zero;
+    const int stop = done ? first_p + 1 : first_zero;
+#pragma unroll
+    for (int k = 0; k < WIN; ++k) excl += (k < stop) ? (v[k] & kValueMask) : 0u;
+    if (done) return excl;
+    if (first_zero < WIN) {
+      const uint32_t w = wait_status(col + (pt - first_zero) * R, error, timeout_ns, polls);
+      excl += w & kValueMask;
+      if (w & kFlagP) return excl;
+      pt -= first_zero + 1;
+    } else {
+      pt -= WIN;
     }
   }
 }
@@ -157,20 +185,15 @@ __device__ __forceinline__ int64_t find_inclusive(const uint32_t* row_flags, int
 template <int W, int R>
 struct TileScratch {
   uint32_t warp_cnt[W][R];  // per-warp digit counters, then per-warp offsets
-#if LSDRS_RANK == 2
-  uint32_t peer_bits[W][R];  // per-warp lane masks of the item being ranked
-#endif
-  uint32_t tile_start[R];  // digit counts, then digit starts in the tile
-  uint32_t g_off[R];       // output position of staged slot j is g_off[d] + j
-  int64_t p_tile;          // look-back result: nearest predecessor with P (or -1)
-  int64_t p_stop;          // counts are summed over tiles (p_stop, t)
+  uint32_t tile_start[R];   // digit counts, then digit starts in the tile
+  uint32_t g_off[R];        // output position of staged slot j is g_off[d] + j
 };
 
 // Where a tile's keys and payloads are read from and staged to.  Key and
 // payload sources are warp-striped: the item at tile position p is src[p].
 template <class KeyOp>
 struct TileIo {
-  const typename KeyOp::T* key_src;  // global
+  const typename KeyOp::T* key_src;  // shared (prefetched) or global
   const uint32_t* val_src;           // shared, global, or null (generate indices)
   typename KeyOp::T* stage_keys;     // shared, TILE keys
   uint32_t* stage_vals;              // shared, TILE words (may equal val_src)
@@ -179,7 +202,7 @@ struct TileIo {
 
 // One tile: rank, publish, look back, stage, write.  Called by every thread
 // of the CTA; begins and ends with all threads converged.
-template <bool FULL, class KeyOp, int BITS, int VK, int THREADS, int ITEMS>
+template <bool FULL, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
 __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
                                            TileScratch<THREADS / kWarp, (1 << BITS)>& s,
                                            const TileIo<KeyOp>& io, int64_t tile, int64_t row,
@@ -196,7 +219,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   const int warp = tid >> 5;
   const int64_t row_base = row * a.cols;
   const int64_t tile_begin = t * TILE;
-  const int64_t row_tile0 = tile - t;  // global index of the row's first tile
+  uint32_t* status_tile = a.status + tile * R;
   const int wpos = warp * WKEYS + lane;  // tile position of item 0
   uint32_t trips = 0, polls = 0;
 #if LSDRS_STATS >= 2
@@ -206,7 +229,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   T keys[ITEMS];
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i)
-    keys[i] = (FULL || wpos + i * kWarp < valid) ? ld_stream(io.key_src + wpos + i * kWarp) : T(0);
+    keys[i] = (FULL || wpos + i * kWarp < valid) ? io.key_src[wpos + i * kWarp] : T(0);
 
   // ---- 3. rank within the warp ------------------------------------------
   // packed[i] = digit << 16 | rank of the item among the warp's keys of
@@ -214,28 +237,14 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   uint32_t packed[ITEMS];
   uint32_t* wc = s.warp_cnt[warp];
   const uint32_t lt = lanemask_lt();
-#if LSDRS_RANK == 2
-  uint32_t* pb = s.peer_bits[warp];
-  const uint32_t lane_bit = 1u << lane;
-#endif
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
     uint32_t d = KeyOp::digit(keys[i], a.shift, a.mask, a.flip);
     if (!FULL && wpos + i * kWarp >= valid) d = R - 1;
-#if LSDRS_RANK == 2
-    atomicOr(pb + d, lane_bit);
-    __syncwarp();
-    const uint32_t peers = pb[d];
-    __syncwarp();
-#else
     const uint32_t peers = digit_peers<BITS>(d);
-#endif
     const int leader = __ffs(peers) - 1;
     uint32_t before = 0;
     if (lane == leader) {
-#if LSDRS_RANK == 2
-      pb[d] = 0;
-#endif
       before = wc[d];
       wc[d] = before + __popc(peers);
     }
@@ -258,11 +267,9 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     }
     s.tile_start[tid] = sum;
     my_count = (!FULL && tid == R - 1) ? sum - static_cast<uint32_t>(TILE - valid) : sum;
-    st_relaxed(a.counts + tile * R + tid, my_count);
-    if (t == 0) st_relaxed(a.incl + tile * R + tid, my_count);
+    st_relaxed(status_tile + tid, (t == 0 ? kFlagP : kFlagA) | my_count);
   }
   __syncthreads();
-  if (tid == 0) st_release(a.flags + tile, t == 0 ? kTileP : kTileA);
   LSDRS_PHASE(1);  // warp offsets + publish
   if (warp == 0) {  // exclusive scan of tile_start over the digits
     constexpr int PER = (R + kWarp - 1) / kWarp;
@@ -287,17 +294,9 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
       if (d < R) s.tile_start[d] = run;
       run += v[k];
     }
-  } else if (warp == W - 1 && t > 0) {  // look-back over the tile flags
-    int64_t stop = 0;
-    const int64_t p = find_inclusive(a.flags + row_tile0, t, a.error, a.timeout_ns, &stop,
-                                     trips, polls);
-    if (lane == 0) {
-      s.p_tile = p;
-      s.p_stop = stop;
-    }
   }
   __syncthreads();
-  LSDRS_PHASE(2);  // digit scan + flag search
+  LSDRS_PHASE(2);  // digit scan
 
   // ---- 5. stage keys, then payloads, in tile-sorted order ---------------
 #pragma unroll
@@ -306,23 +305,6 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     const uint32_t pos = s.tile_start[d] + s.warp_cnt[warp][d] + (packed[i] & 0xFFFFu);
     io.stage_keys[pos] = keys[i];
     packed[i] = pos;  // keep the staging slot for the payload
-  }
-  // prefix of digit tid over the row's earlier tiles: the P tile's inclusive
-  // prefix plus the counts of the tiles after it (loads issued together)
-  uint32_t excl = 0;
-  if (tid < R && t > 0) {
-    const int64_t p = s.p_tile;
-    const int64_t stop = s.p_stop;
-    if (p >= 0) excl = ld_relaxed(a.incl + (row_tile0 + p) * R + tid);
-    const uint32_t* c = a.counts + row_tile0 * R + tid;
-    int64_t k = stop + 1;
-    for (; k + 3 < t; k += 4) {
-      const uint32_t c0 = ld_relaxed(c + k * R), c1 = ld_relaxed(c + (k + 1) * R);
-      const uint32_t c2 = ld_relaxed(c + (k + 2) * R), c3 = ld_relaxed(c + (k + 3) * R);
-      excl += (c0 + c1) + (c2 + c3);
-    }
-    for (; k < t; ++k) excl += ld_relaxed(c + k * R);
-    st_relaxed(a.incl + tile * R + tid, excl + my_count);
   }
   if constexpr (kVals) {
     if (io.val_bar != nullptr && !mbar_wait_bounded(io.val_bar, 0, a.timeout_ns)) {
@@ -344,16 +326,26 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) io.stage_vals[packed[i]] = v[i];
   }
-  if (tid < R) s.g_off[tid] = a.bases[row * a.bases_row_stride + tid] + excl - s.tile_start[tid];
+  LSDRS_PHASE(3);  // staging (thread 0's share)
+
+  // ---- 6. decoupled look-back -------------------------------------------
+  if (tid < R) {
+    uint32_t excl = 0;
+    if (t > 0) {
+      excl = look_back<R, WIN>(a.status + (tile - t) * R + tid, t, a.error, a.timeout_ns, trips, polls);
+      st_relaxed(status_tile + tid, kFlagP | (excl + my_count));
+    }
+    s.g_off[tid] = a.bases[row * a.bases_row_stride + tid] + excl - s.tile_start[tid];
+  }
+  LSDRS_PHASE(4);  // thread 0's look-back
 #if LSDRS_STATS
   if (trips) atomicAdd(a.error + kStatsWord, trips);
   if (polls) atomicAdd(a.error + kStatsWord + 1, polls);
 #endif
   __syncthreads();
-  if (tid == 0 && t > 0) st_release(a.flags + tile, kTileP);
-  LSDRS_PHASE(3);  // staging + prefix sums
+  LSDRS_PHASE(5);  // wait for the slowest digit's look-back
 
-  // ---- 6. contiguous per-digit runs out ---------------------------------
+  // ---- 7. contiguous per-digit runs out ---------------------------------
   T* kout = static_cast<T*>(a.keys_out) + row_base;
   uint32_t* vout32 = static_cast<uint32_t*>(a.vals_out) + row_base;
   int64_t* vout64 = static_cast<int64_t*>(a.vals_out) + row_base;
@@ -375,23 +367,39 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
       }
     }
   }
-  LSDRS_PHASE(4);  // write-out
+  LSDRS_PHASE(6);  // write-out
 }
 
+struct TilePlace {
+  int64_t row, t, tile_begin;
+  int valid;
+};
+
+template <int TILE>
+__device__ __forceinline__ TilePlace place_tile(const SweepArgs& a, int64_t tile) {
+  TilePlace p;
+  p.row = tile / a.tiles_per_row;
+  p.t = tile - p.row * a.tiles_per_row;
+  p.tile_begin = p.t * TILE;
+  p.valid = static_cast<int>(a.cols - p.tile_begin < TILE ? a.cols - p.tile_begin : TILE);
+  return p;
+}
+
+// The grid has one CTA per tile.
 template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS>
 struct SweepSmem {
   using T = typename KeyOp::T;
   static constexpr int kTile = THREADS * ITEMS;
   static constexpr bool kVals = VK != kValNone;
-  alignas(128) T keys[kTile];                     // key stage
-  alignas(128) uint32_t vals[kVals ? kTile : 4];  // payloads in, then payload stage
+  alignas(128) T keys[kTile];                      // key stage
+  alignas(128) uint32_t vals[kVals ? kTile : 4];   // payloads in, then payload stage
   TileScratch<THREADS / kWarp, (1 << BITS)> scratch;
   uint64_t bar;
   uint32_t tile_id;
   uint32_t abort;
 };
 
-template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB>
+template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB, int WIN>
 __global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
   using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
   using T = typename KeyOp::T;
@@ -399,7 +407,6 @@ __global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
   constexpr int W = THREADS / kWarp;
   constexpr int TILE = S::kTile;
   static_assert(R <= THREADS, "one thread per digit");
-  static_assert(W >= 2, "the digit scan and the flag search run on different warps");
   static_assert(kWarp * ITEMS < 65536, "ranks are packed in 16 bits");
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -410,64 +417,52 @@ __global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
     s.tile_id = atomicAdd(a.tile_counter, 1u);
     s.abort = ld_relaxed(a.error) != kErrNone;
   }
-  for (int i = tid; i < W * R; i += THREADS) {
-    (&s.scratch.warp_cnt[0][0])[i] = 0;
-#if LSDRS_RANK == 2
-    (&s.scratch.peer_bits[0][0])[i] = 0;
-#endif
-  }
+  for (int i = tid; i < W * R; i += THREADS) (&s.scratch.warp_cnt[0][0])[i] = 0;
   __syncthreads();
 
   const int64_t tile = s.tile_id;
-  const int64_t row = tile / a.tiles_per_row;
-  const int64_t t = tile - row * a.tiles_per_row;
-  const int64_t tile_begin = t * TILE;
-  const int valid = static_cast<int>(a.cols - tile_begin < TILE ? a.cols - tile_begin : TILE);
-  const int64_t off = row * a.cols + tile_begin;
-
+  const TilePlace p = place_tile<TILE>(a, tile);
+  const int64_t off = p.row * a.cols + p.tile_begin;
   TileIo<KeyOp> io;
   io.key_src = static_cast<const T*>(a.keys_in) + off;
   io.stage_keys = s.keys;
   io.stage_vals = s.vals;
   io.val_src = nullptr;
   io.val_bar = nullptr;
-  if (s.abort) {
-    // An earlier tile failed: publish zero prefixes so that later tiles stop
-    // here (their prefixes are then underestimates: wrong but in bounds).
-    if (tid < R) {
-      st_relaxed(a.counts + tile * R + tid, 0u);
-      st_relaxed(a.incl + tile * R + tid, 0u);
-    }
-    __syncthreads();
-    if (tid == 0) st_release(a.flags + tile, kTileP);
-    return;
-  }
-  if (VK != kValNone && a.vals_in != nullptr) {
-    // Payloads are not needed before the staging step: a full tile with an
-    // aligned source gets them by one bulk copy issued now.
-    const uint32_t* vsrc = static_cast<const uint32_t*>(a.vals_in) + off;
-    io.val_src = vsrc;
-    if (LSDRS_VALS_TMA && valid == TILE && (reinterpret_cast<uintptr_t>(vsrc) & 15) == 0) {
-      if (tid == 0) {
-        mbar_init(&s.bar, 1);
-        mbar_arrive_expect_tx(&s.bar, TILE * sizeof(uint32_t));
-        bulk_copy_g2s(s.vals, vsrc, TILE * sizeof(uint32_t), &s.bar);
-      }
-      io.val_src = s.vals;
-      io.val_bar = &s.bar;  // the first barrier in the tile orders the init
-    }
-  }
-  if (valid == TILE) {
-    sweep_tile<true, KeyOp, BITS, VK, THREADS, ITEMS>(a, s.scratch, io, tile, row, t, valid);
+  if (s.abort) {  // an earlier tile failed: release successors and stop
+    if (tid < R) st_relaxed(a.status + tile * R + tid, kFlagP);
   } else {
-    sweep_tile<false, KeyOp, BITS, VK, THREADS, ITEMS>(a, s.scratch, io, tile, row, t, valid);
+    if (VK != kValNone && a.vals_in != nullptr) {
+      // Payloads are not needed before the staging step: a full tile with an
+      // aligned source gets them by one bulk copy issued now; the tile's
+      // first block-wide barrier orders the barrier's initialisation before
+      // any thread waits on it.
+      const uint32_t* vsrc = static_cast<const uint32_t*>(a.vals_in) + off;
+      io.val_src = vsrc;
+      if (LSDRS_VALS_TMA && p.valid == TILE && (reinterpret_cast<uintptr_t>(vsrc) & 15) == 0) {
+        if (tid == 0) {
+          mbar_init(&s.bar, 1);
+          mbar_arrive_expect_tx(&s.bar, TILE * sizeof(uint32_t));
+          bulk_copy_g2s(s.vals, vsrc, TILE * sizeof(uint32_t), &s.bar);
+        }
+        io.val_src = s.vals;
+        io.val_bar = &s.bar;
+      }
+    }
+    if (p.valid == TILE)
+      sweep_tile<true, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io, tile, p.row, p.t,
+                                                             p.valid);
+    else
+      sweep_tile<false, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io, tile, p.row, p.t,
+                                                              p.valid);
   }
+  if (a.status_zero != nullptr && tid < R) a.status_zero[tile * R + tid] = 0;
 }
 
-template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB>
+template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB, int WIN>
 cudaError_t launch_sweep_t(const SweepArgs& a, int64_t grid, cudaStream_t s) {
   using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
-  auto kern = onesweep_kernel<KeyOp, BITS, VK, THREADS, ITEMS, MINB>;
+  auto kern = onesweep_kernel<KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>;
   const size_t smem = sizeof(S);
   if (smem > 48 * 1024) {
     cudaError_t e =
@@ -478,17 +473,17 @@ cudaError_t launch_sweep_t(const SweepArgs& a, int64_t grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <class KeyOp, int VK, int THREADS, int ITEMS, int MINB>
+template <class KeyOp, int VK, int THREADS, int ITEMS, int MINB, int WIN>
 cudaError_t launch_sweep_bits(int bits, const SweepArgs& a, int64_t grid, cudaStream_t s) {
   switch (bits) {
-    case 1: return launch_sweep_t<KeyOp, 1, VK, THREADS, ITEMS, MINB>(a, grid, s);
-    case 2: return launch_sweep_t<KeyOp, 2, VK, THREADS, ITEMS, MINB>(a, grid, s);
-    case 3: return launch_sweep_t<KeyOp, 3, VK, THREADS, ITEMS, MINB>(a, grid, s);
-    case 4: return launch_sweep_t<KeyOp, 4, VK, THREADS, ITEMS, MINB>(a, grid, s);
-    case 5: return launch_sweep_t<KeyOp, 5, VK, THREADS, ITEMS, MINB>(a, grid, s);
-    case 6: return launch_sweep_t<KeyOp, 6, VK, THREADS, ITEMS, MINB>(a, grid, s);
-    case 7: return launch_sweep_t<KeyOp, 7, VK, THREADS, ITEMS, MINB>(a, grid, s);
-    case 8: return launch_sweep_t<KeyOp, 8, VK, THREADS, ITEMS, MINB>(a, grid, s);
+    case 1: return launch_sweep_t<KeyOp, 1, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
+    case 2: return launch_sweep_t<KeyOp, 2, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
+    case 3: return launch_sweep_t<KeyOp, 3, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
+    case 4: return launch_sweep_t<KeyOp, 4, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
+    case 5: return launch_sweep_t<KeyOp, 5, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
+    case 6: return launch_sweep_t<KeyOp, 6, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
+    case 7: return launch_sweep_t<KeyOp, 7, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
+    case 8: return launch_sweep_t<KeyOp, 8, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
