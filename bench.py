@@ -239,6 +239,7 @@ def main():
     ap.add_argument("--no-distributions", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-copy-probe", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -314,12 +315,32 @@ def main():
     roofline = {"bound": "hbm", "kernel": "onesweep (one scatter pass)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_source": f"{peak_kind} hbm_gbs (copy, burst)",
+                "copy_probe_gbs": None,
                 "traffic": recorded_traffic(n),
                 "algorithmic_bytes_per_launch": sweep_bytes_per_launch(n, KEY_BYTES, VAL_BYTES),
                 "avg_launch_ms": sweep_avg}
     kernels = {k: {"launches": c, "total_ms": t, "share": t / max(sum(x[1] for x in
                                                                       per_kernel.values()), 1e-9)}
                for k, (c, t) in per_kernel.items()}
+
+    # ---- the copy probe: this build's own streaming copy on the same GPU ----
+    copy_gbs = None
+    if not args.no_copy_probe:
+        src = torch.empty(1 << 31, dtype=torch.uint8, device=dev)  # 2 GiB, > L2
+        dst = torch.empty_like(src)
+        for _ in range(3):
+            rs.copy_probe(dst, src)
+        torch.cuda.synchronize()
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(10):
+            rs.copy_probe(dst, src)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        copy_gbs = 2 * src.numel() / (c0.elapsed_time(c1) / 10 * 1e-3) / 1e9
+        rs.profile_read()
+        del src, dst
 
     # ---- end to end through host buffers ---------------------------------
     e2e = None
@@ -378,6 +399,7 @@ def main():
                "sample": f"2^{args.cpu_log2} keys of the same uniform u32 key-value workload, "
                          f"one sort, {secs:.1f} s on one host thread"}
 
+    roofline["copy_probe_gbs"] = copy_gbs
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "Gkeys/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
