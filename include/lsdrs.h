@@ -191,6 +191,23 @@ int rs_profile_read(rs_kernel_time* out, int max);
  * count for measurement); resets the counter. */
 uint64_t rs_launch_count_reset(void);
 
+/* Key-value sort for callers that cannot allocate device memory (the pages
+ * have no counterpart of this entry point).  Same result and arguments as
+ * radix_sort_pairs_u32 without temp/temp_bytes: the scratch is a fixed 4 MiB
+ * array inside the library's device code, which every GPU that loads the
+ * library holds until the process exits.
+ *   n         0 <= n <= 262,144 (2^18); larger n returns RS_ERR_INVALID
+ *             before anything is enqueued
+ * The first call on a device looks up that device's address of the array
+ * (make it before any stream capture on that device).  Every call on a device
+ * shares the one array: calls whose work overlaps on the GPU (for example on
+ * two streams) race and give wrong results; calls on one stream are safe.
+ * Each call clears what it needs cleared; nothing else is allocated or freed. */
+rs_status radix_sort_pairs_u32_noalloc(const uint32_t* keys_in, uint32_t* keys_out,
+                                       const uint32_t* vals_in, uint32_t* vals_out, size_t n,
+                                       int begin_bit, int end_bit, int digit_bits,
+                                       void* stream);
+
 #ifdef __cplusplus
 }
 #endif

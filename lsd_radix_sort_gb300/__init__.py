@@ -37,6 +37,7 @@ EXPORTED_SYMBOLS = (
     "radix_segmented_sort_f16", "radix_sort_histograms", "radix_sort_device_status",
     "rs_status_string", "rs_set_lookback_timeout_ns", "rs_lookback_timeout_probe",
     "rs_copy_probe", "rs_profile_enable", "rs_profile_read", "rs_launch_count_reset",
+    "radix_sort_pairs_u32_noalloc",
 )
 
 
@@ -92,6 +93,7 @@ def load_library() -> ctypes.CDLL:
             "rs_lookback_timeout_probe": [P, u64, P, P],
             "rs_copy_probe": [P, P, sz, P],
             "rs_profile_enable": [i],
+            "radix_sort_pairs_u32_noalloc": [P, P, P, P, sz, i, i, i, P],
         }
         for name, args in sig.items():
             f = getattr(lib, name)

@@ -452,3 +452,57 @@ int rs_profile_read(rs_kernel_time* out, int max) {
 uint64_t rs_launch_count_reset(void) { return g_launches.exchange(0); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Key-value sort that allocates nothing.
+//
+// Some callers cannot allocate device memory at the point where they sort:
+// code that runs inside a stream capture, callers whose memory is owned by a
+// pool they may not grow, or plugins that are handed only the buffers they
+// work on.  For them the scratch of the sort lives in one fixed array in this
+// library's device image.  The array is created when the library's device
+// code is loaded and stays until the process exits, on every GPU that loads
+// the library, so it is kept small: sorts of at most kNoAllocMaxKeys keys.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr size_t kNoAllocMaxKeys = size_t(1) << 18;     // 262,144 keys
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB per GPU
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kNoAllocMaxDevices] = {};
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+extern "C" rs_status radix_sort_pairs_u32_noalloc(const uint32_t* keys_in, uint32_t* keys_out,
+                                                  const uint32_t* vals_in, uint32_t* vals_out,
+                                                  size_t n, int begin_bit, int end_bit,
+                                                  int digit_bits, void* stream) {
+  if (n > kNoAllocMaxKeys) return RS_ERR_INVALID;
+  Plan p;
+  rs_status st = make_plan(kKeyU32, kValU32, 1, static_cast<int64_t>(n), begin_bit, end_bit,
+                           digit_bits, &p);
+  if (st != RS_OK) return st;
+  if (p.total > kNoAllocScratchBytes) return RS_ERR_INVALID;
+  if (n == 0) return RS_OK;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RS_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return RS_ERR_INVALID;
+  void* scratch = nullptr;
+  {
+    // The host-side name of the array is not a device address: look the
+    // address up once per device, with that device current.
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr)
+        return RS_ERR_CUDA;
+      g_noalloc_addr[dev] = addr;
+    }
+    scratch = g_noalloc_addr[dev];
+  }
+  // The sort's first kernel zeroes every part of the scratch that must start
+  // at zero, so what an earlier call left there does not matter.
+  return run_sort(p, keys_in, keys_out, vals_in, vals_out, 0u, scratch, kNoAllocScratchBytes,
+                  static_cast<cudaStream_t>(stream));
+}

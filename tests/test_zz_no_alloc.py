@@ -1,0 +1,52 @@
+"""The key-value sort for callers that cannot allocate device memory.
+
+Code that sorts inside a stream capture, or that is handed only its input
+and output buffers, cannot ask the driver for scratch.  The no-allocation
+entry point keeps its scratch in a fixed array of the library's device code
+instead; it must give exactly what the ordinary entry point gives, call after
+call, although every call reuses (and finds dirty) the same array.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from lsd_radix_sort_gb300 import workloads
+from tests.gpu_util import poisoned_like, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+MAX_KEYS = 1 << 18
+
+
+def call_noalloc(lib, dk, dv, ko, vo, n, begin=0, end=32, bits=8):
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return lib.radix_sort_pairs_u32_noalloc(
+        ctypes.c_void_p(dk.data_ptr()), ctypes.c_void_p(ko.data_ptr()),
+        ctypes.c_void_p(dv.data_ptr()), ctypes.c_void_p(vo.data_ptr()),
+        n, begin, end, bits, stream)
+
+
+@pytest.mark.parametrize("n,begin,end,bits", [(100_003, 0, 32, 8), (MAX_KEYS, 0, 32, 4),
+                                              (4097, 3, 29, 7)])
+def test_no_alloc_matches_ordinary_sort_twice(rs, n, begin, end, bits):
+    lib = rs.load_library()
+    for call, seed in enumerate((1, 2)):  # two calls in a row, different data
+        keys = workloads.u32_uniform(n, seed)
+        keys[::5] = keys[0]
+        vals = workloads.index_payload(n)
+        dk, dv = to_dev(keys), to_dev(vals)
+        ko, vo = poisoned_like(dk), poisoned_like(dv)
+        assert call_noalloc(lib, dk, dv, ko, vo, n, begin, end, bits) == rs.RS_OK
+        ek, ev = rs.radix_sort_pairs(dk, dv, begin_bit=begin, end_bit=end, digit_bits=bits)
+        torch.cuda.synchronize()
+        assert np.array_equal(to_host(ko, np.uint32), to_host(ek, np.uint32)), f"call {call}"
+        assert np.array_equal(to_host(vo, np.uint32), to_host(ev, np.uint32)), f"call {call}"
+
+
+def test_no_alloc_rejects_beyond_its_maximum(rs):
+    lib = rs.load_library()
+    d = torch.empty(4, dtype=torch.int32, device="cuda")
+    assert call_noalloc(lib, d, d, d, d, MAX_KEYS + 1) == rs.RS_ERR_INVALID
+    assert call_noalloc(lib, d, d, d, d, 0) == rs.RS_OK
