@@ -96,10 +96,18 @@ __device__ __forceinline__ uint32_t digit_peers(uint32_t d) {
   uint32_t peers = kFull;
 #pragma unroll
   for (int b = 0; b < BITS; ++b) {
-    // m: all ones when bit b of d is set; the peers agree with m on bit b.
-    const uint32_t m = static_cast<uint32_t>(static_cast<int32_t>(d << (31 - b)) >> 31);
-    const uint32_t votes = __ballot_sync(kFull, m);
-    peers &= ~(votes ^ m);
+    // Vote on bit b; lanes whose bit is clear keep the complement of the
+    // votes.  Written with the predicate explicit, the test, the vote and
+    // the conditional complement stay about three instructions per bit.
+    uint32_t agree;
+    asm("{\n\t.reg .pred p;\n\t.reg .b32 t;\n\t"
+        "and.b32 t, %1, %2;\n\t"
+        "setp.ne.u32 p, t, 0;\n\t"
+        "vote.sync.ballot.b32 %0, p, 0xffffffff;\n\t"
+        "@!p not.b32 %0, %0;\n\t}"
+        : "=r"(agree)
+        : "r"(d), "r"(1u << b));
+    peers &= agree;
   }
   return peers;
 #endif
@@ -155,26 +163,20 @@ __device__ __forceinline__ uint32_t look_back(const uint32_t* col, int64_t t, ui
 #pragma unroll
     for (int k = 0; k < WIN; ++k) v[k] = (pt - k >= 0) ? ld_relaxed(col + (pt - k) * R) : kFlagP;
     ++trips;
-    uint32_t zero_mask = 0, p_mask = 0;
+    // consume the window in order up to the first inclusive prefix (done),
+    // or up to the first word not yet published (wait for it)
+    int k = 0;
 #pragma unroll
-    for (int k = 0; k < WIN; ++k) {
-      zero_mask |= (v[k] == 0 ? 1u : 0u) << k;
-      p_mask |= (v[k] >> 31) << k;
+    for (; k < WIN; ++k) {
+      if (v[k] == 0) break;
+      excl += v[k] & kValueMask;
+      if (v[k] & kFlagP) return excl;
     }
-    // consume words [0, stop): up to and including the first P, or up to
-    // (not including) the first unpublished word, whichever comes first.
-    const int first_p = p_mask ? __ffs(p_mask) - 1 : WIN;
-    const int first_zero = zero_mask ? __ffs(zero_mask) - 1 : WIN;
-    const bool done = first_p < first_zero;
-    const int stop = done ? first_p + 1 : first_zero;
-#pragma unroll
-    for (int k = 0; k < WIN; ++k) excl += (k < stop) ? (v[k] & kValueMask) : 0u;
-    if (done) return excl;
-    if (first_zero < WIN) {
-      const uint32_t w = wait_status(col + (pt - first_zero) * R, error, timeout_ns, polls);
+    if (k < WIN) {
+      const uint32_t w = wait_status(col + (pt - k) * R, error, timeout_ns, polls);
       excl += w & kValueMask;
       if (w & kFlagP) return excl;
-      pt -= first_zero + 1;
+      pt -= k + 1;
     } else {
       pt -= WIN;
     }
