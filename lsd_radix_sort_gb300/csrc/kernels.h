@@ -28,15 +28,15 @@ struct SweepShape {
 // are the fastest measured on GB300 for 2^28-key sorts.
 #ifndef LSDRS_U32K_T
 #define LSDRS_U32K_T 256
-#define LSDRS_U32K_I 24
-#define LSDRS_U32K_B 4
+#define LSDRS_U32K_I 32
+#define LSDRS_U32K_B 3
 #endif
 #ifndef LSDRS_U32K_W
 #define LSDRS_U32K_W 8
 #endif
 #ifndef LSDRS_U32P_T
 #define LSDRS_U32P_T 256
-#define LSDRS_U32P_I 16
+#define LSDRS_U32P_I 20
 #define LSDRS_U32P_B 4
 #endif
 #ifndef LSDRS_U32P_W
@@ -44,16 +44,16 @@ struct SweepShape {
 #endif
 #ifndef LSDRS_U64K_T
 #define LSDRS_U64K_T 256
-#define LSDRS_U64K_I 12
-#define LSDRS_U64K_B 4
+#define LSDRS_U64K_I 16
+#define LSDRS_U64K_B 3
 #endif
 #ifndef LSDRS_U64K_W
 #define LSDRS_U64K_W 4
 #endif
 #ifndef LSDRS_U64P_T
 #define LSDRS_U64P_T 256
-#define LSDRS_U64P_I 12
-#define LSDRS_U64P_B 4
+#define LSDRS_U64P_I 16
+#define LSDRS_U64P_B 3
 #endif
 #ifndef LSDRS_U64P_W
 #define LSDRS_U64P_W 4

@@ -11,7 +11,7 @@ from tests.gpu_util import field, poisoned_like, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
-TILE_U32_KEYS, TILE_U32_PAIRS, TILE_U64, TILE_F16 = 8192, 6144, 4096, 4096
+TILE_U32_KEYS, TILE_U32_PAIRS, TILE_U64, TILE_F16 = 8192, 5120, 4096, 4096
 
 
 def run_keys(rs, keys, begin=0, end=None, bits=8):
