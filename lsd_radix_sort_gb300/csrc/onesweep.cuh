@@ -156,12 +156,20 @@ __device__ __forceinline__ uint32_t look_back(const uint32_t* col, int64_t t, ui
                                               uint64_t timeout_ns, uint32_t& trips,
                                               uint32_t& polls) {
   static_assert(WIN >= 1 && WIN <= 32, "window of 1..32 tiles");
-  uint32_t excl = 0;
-  int64_t pt = t - 1;  // newest predecessor not yet consumed
+  // Raw words are summed: the flag bits sit above bit 29 and the true sum
+  // of the counts stays below 2^30, so masking once at the end is exact.
+  uint32_t raw = 0;
+  int pt = static_cast<int>(t) - 1;  // newest predecessor not yet consumed
   for (;;) {
+    const uint32_t* p = col + static_cast<int64_t>(pt) * R;  // word of tile pt
     uint32_t v[WIN];
+    if (pt >= WIN - 1) {
 #pragma unroll
-    for (int k = 0; k < WIN; ++k) v[k] = (pt - k >= 0) ? ld_relaxed(col + (pt - k) * R) : kFlagP;
+      for (int k = 0; k < WIN; ++k) v[k] = ld_relaxed(p - k * R);
+    } else {
+#pragma unroll
+      for (int k = 0; k < WIN; ++k) v[k] = k <= pt ? ld_relaxed(p - k * R) : kFlagP;
+    }
     ++trips;
     // consume the window in order up to the first inclusive prefix (done),
     // or up to the first word not yet published (wait for it)
@@ -169,13 +177,13 @@ __device__ __forceinline__ uint32_t look_back(const uint32_t* col, int64_t t, ui
 #pragma unroll
     for (; k < WIN; ++k) {
       if (v[k] == 0) break;
-      excl += v[k] & kValueMask;
-      if (v[k] & kFlagP) return excl;
+      raw += v[k];
+      if (static_cast<int32_t>(v[k]) < 0) return raw & kValueMask;  // flag P
     }
     if (k < WIN) {
-      const uint32_t w = wait_status(col + (pt - k) * R, error, timeout_ns, polls);
-      excl += w & kValueMask;
-      if (w & kFlagP) return excl;
+      const uint32_t w = wait_status(p - k * R, error, timeout_ns, polls);
+      raw += w;
+      if (w & kFlagP) return raw & kValueMask;
       pt -= k + 1;
     } else {
       pt -= WIN;
@@ -244,9 +252,11 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     uint32_t d = KeyOp::digit(keys[i], a.shift, a.mask, a.flip);
     if (!FULL && wpos + i * kWarp >= valid) d = R - 1;
     const uint32_t peers = digit_peers<BITS>(d);
-    const int leader = __ffs(peers) - 1;
+    // the highest peer lane advances the counter (one find-leading-bit)
+    uint32_t leader;
+    asm("bfind.u32 %0, %1;" : "=r"(leader) : "r"(peers));
     uint32_t before = 0;
-    if (lane == leader) {
+    if (static_cast<uint32_t>(lane) == leader) {
       before = wc[d];
       wc[d] = before + __popc(peers);
     }
