@@ -308,13 +308,21 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     }
   }
   __syncthreads();
+  // fold the digit starts into the per-warp offsets: staging then reads one
+  // word per key (conflict-free here: thread d walks column d)
+  if (tid < R) {
+    const uint32_t start = s.tile_start[tid];
+#pragma unroll
+    for (int w = 0; w < W; ++w) s.warp_cnt[w][tid] += start;
+  }
+  __syncthreads();
   LSDRS_PHASE(2);  // digit scan
 
   // ---- 5. stage keys, then payloads, in tile-sorted order ---------------
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
     const uint32_t d = packed[i] >> 16;
-    const uint32_t pos = s.tile_start[d] + s.warp_cnt[warp][d] + (packed[i] & 0xFFFFu);
+    const uint32_t pos = s.warp_cnt[warp][d] + (packed[i] & 0xFFFFu);
     io.stage_keys[pos] = keys[i];
     packed[i] = pos;  // keep the staging slot for the payload
   }
