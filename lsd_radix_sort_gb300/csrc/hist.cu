@@ -38,19 +38,89 @@ struct HistCfg {
   }
 };
 
-template <class KeyOp, int BITS>
-__device__ __forceinline__ void count_key(uint32_t* cnt_col, typename KeyOp::T k, int begin_bit,
-                                          int passes, uint32_t last_mask, uint32_t flip) {
+// Per-thread view of the counters: shift and mask of every pass held in
+// registers; ALL = every pass of the key type is present (the usual case),
+// which drops the per-pass bound test.
+template <class KeyOp, int BITS, bool ALL>
+struct KeyCounter {
   using Cfg = HistCfg<KeyOp, BITS>;
-  constexpr int R = Cfg::kRadix;
-  constexpr int C = Cfg::kCols;
+  static constexpr int R = Cfg::kRadix;
+  static constexpr int C = Cfg::kCols;
+  static constexpr int MP = Cfg::kMaxPasses;
+  // many narrow passes (digits of 1-3 bits) would not fit in registers:
+  // those compute shift and mask per key instead
+  static constexpr bool kHeld = MP <= 16;
+  static constexpr int MH = kHeld ? MP : 1;
+  uint32_t* col;
+  int begin_bit, passes;
+  uint32_t last_mask, flip;
+  int shift[MH];
+  uint32_t mask[MH];
+
+  __device__ __forceinline__ KeyCounter(uint32_t* c, int b, int np, uint32_t lm, uint32_t f)
+      : col(c), begin_bit(b), passes(np), last_mask(lm), flip(f) {
 #pragma unroll
-  for (int p = 0; p < Cfg::kMaxPasses; ++p) {
-    if (p < passes) {
-      const uint32_t mask = p == passes - 1 ? last_mask : static_cast<uint32_t>(R - 1);
-      const uint32_t d = KeyOp::digit(k, begin_bit + p * BITS, mask, flip);
-      atomicAdd(cnt_col + (p * R + d) * C, 1u);
+    for (int p = 0; p < MH; ++p) {
+      shift[p] = b + p * BITS;
+      mask[p] = p == np - 1 ? lm : static_cast<uint32_t>(R - 1);
     }
+  }
+  __device__ __forceinline__ void add(typename KeyOp::T k) const {
+    if constexpr (kHeld) {
+#pragma unroll
+      for (int p = 0; p < MP; ++p) {
+        if (ALL || p < passes) {
+          const uint32_t d = KeyOp::digit(k, shift[p], mask[p], flip);
+          atomicAdd(col + (p * R + d) * C, 1u);
+        }
+      }
+    } else {
+      for (int p = 0; p < passes; ++p) {
+        const uint32_t m = p == passes - 1 ? last_mask : static_cast<uint32_t>(R - 1);
+        const uint32_t d = KeyOp::digit(k, begin_bit + p * BITS, m, flip);
+        atomicAdd(col + (p * R + d) * C, 1u);
+      }
+    }
+  }
+};
+
+// Counts keys [begin, end) of one row slice: a scalar head up to 16-byte
+// alignment, a vectorised body (U 16-byte loads in flight per thread) and a
+// scalar tail.
+template <class KeyOp, int BITS, bool ALL>
+__device__ __forceinline__ void count_range(const typename KeyOp::T* base, int64_t begin,
+                                            int64_t end, const KeyCounter<KeyOp, BITS, ALL>& c) {
+  using T = typename KeyOp::T;
+  using Cfg = HistCfg<KeyOp, BITS>;
+  constexpr int V = Cfg::kVec;
+  constexpr int U = Cfg::kUnroll;
+  const int tid = threadIdx.x;
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(base + begin);
+  int64_t head = static_cast<int64_t>(((16 - (addr & 15)) & 15) / sizeof(T));
+  if (head > end - begin) head = end - begin;
+  const int64_t body_begin = begin + head;
+  const int64_t nvec = (end - body_begin) / V;
+  const int64_t body_end = body_begin + nvec * V;
+  if (tid < head) c.add(base[begin + tid]);
+  if (tid < end - body_end) c.add(base[body_end + tid]);
+  const uint4* vp = reinterpret_cast<const uint4*>(base + body_begin);
+  int64_t v = tid;
+  for (; v + (U - 1) * kHistThreads < nvec; v += U * kHistThreads) {
+    uint4 buf[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) buf[u] = __ldcs(vp + v + u * kHistThreads);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const T* ks = reinterpret_cast<const T*>(&buf[u]);
+#pragma unroll
+      for (int e = 0; e < V; ++e) c.add(ks[e]);
+    }
+  }
+  for (; v < nvec; v += kHistThreads) {
+    uint4 b = __ldcs(vp + v);
+    const T* ks = reinterpret_cast<const T*>(&b);
+#pragma unroll
+    for (int e = 0; e < V; ++e) c.add(ks[e]);
   }
 }
 
@@ -60,8 +130,6 @@ __global__ void __launch_bounds__(kHistThreads, 1) upfront_hist_kernel(HistArgs 
   using Cfg = HistCfg<KeyOp, BITS>;
   constexpr int R = Cfg::kRadix;
   constexpr int C = Cfg::kCols;
-  constexpr int V = Cfg::kVec;
-  constexpr int U = Cfg::kUnroll;
   extern __shared__ __align__(16) uint32_t cnt[];
 
   const int tid = threadIdx.x;
@@ -83,41 +151,13 @@ __global__ void __launch_bounds__(kHistThreads, 1) upfront_hist_kernel(HistArgs 
   const int64_t end = begin + a.chunk_len < a.cols ? begin + a.chunk_len : a.cols;
   const T* base = static_cast<const T*>(a.keys) + row * a.cols;
   uint32_t* col = cnt + (tid & (C - 1));
-  const int begin_bit = a.begin_bit, passes = a.passes;
-  const uint32_t last_mask = a.last_mask, flip = a.flip;
-
   if (begin < end) {
-    // Split [begin, end) into a scalar head up to 16-byte alignment, a
-    // vectorised body and a scalar tail.
-    const uintptr_t addr = reinterpret_cast<uintptr_t>(base + begin);
-    int64_t head = static_cast<int64_t>(((16 - (addr & 15)) & 15) / sizeof(T));
-    if (head > end - begin) head = end - begin;
-    const int64_t body_begin = begin + head;
-    const int64_t nvec = (end - body_begin) / V;
-    const int64_t body_end = body_begin + nvec * V;
-    if (tid < head) count_key<KeyOp, BITS>(col, base[begin + tid], begin_bit, passes, last_mask, flip);
-    if (tid < end - body_end)
-      count_key<KeyOp, BITS>(col, base[body_end + tid], begin_bit, passes, last_mask, flip);
-
-    const uint4* vp = reinterpret_cast<const uint4*>(base + body_begin);
-    int64_t v = tid;
-    for (; v + (U - 1) * kHistThreads < nvec; v += U * kHistThreads) {
-      uint4 buf[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) buf[u] = __ldcs(vp + v + u * kHistThreads);
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const T* ks = reinterpret_cast<const T*>(&buf[u]);
-#pragma unroll
-        for (int e = 0; e < V; ++e)
-          count_key<KeyOp, BITS>(col, ks[e], begin_bit, passes, last_mask, flip);
-      }
-    }
-    for (; v < nvec; v += kHistThreads) {
-      uint4 b = __ldcs(vp + v);
-      const T* ks = reinterpret_cast<const T*>(&b);
-#pragma unroll
-      for (int e = 0; e < V; ++e) count_key<KeyOp, BITS>(col, ks[e], begin_bit, passes, last_mask, flip);
+    if (a.passes == Cfg::kMaxPasses) {
+      const KeyCounter<KeyOp, BITS, true> c(col, a.begin_bit, a.passes, a.last_mask, a.flip);
+      count_range<KeyOp, BITS, true>(base, begin, end, c);
+    } else {
+      const KeyCounter<KeyOp, BITS, false> c(col, a.begin_bit, a.passes, a.last_mask, a.flip);
+      count_range<KeyOp, BITS, false>(base, begin, end, c);
     }
   }
   __syncthreads();

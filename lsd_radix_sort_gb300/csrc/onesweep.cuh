@@ -62,6 +62,11 @@
 #ifndef LSDRS_STATS
 #define LSDRS_STATS 0
 #endif
+// Stage a 4-byte key with its 4-byte payload as one 8-byte word (one
+// scattered shared store per key instead of two).
+#ifndef LSDRS_STAGE64
+#define LSDRS_STAGE64 0
+#endif
 
 namespace lsdrs {
 
@@ -207,6 +212,7 @@ struct TileIo {
   const uint32_t* val_src;           // shared, global, or null (generate indices)
   typename KeyOp::T* stage_keys;     // shared, TILE keys
   uint32_t* stage_vals;              // shared, TILE words (may equal val_src)
+  uint2* stage_pairs;                // shared, TILE (key, payload) words when paired
   uint64_t* val_bar;                 // completes when a bulk copy filled val_src
 };
 
@@ -319,6 +325,22 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   LSDRS_PHASE(2);  // digit scan
 
   // ---- 5. stage keys, then payloads, in tile-sorted order ---------------
+  constexpr bool kPair64 = LSDRS_STAGE64 && kVals && sizeof(T) == 4;
+  if constexpr (kPair64) {
+    if (io.val_bar != nullptr && !mbar_wait_bounded(io.val_bar, 0, a.timeout_ns)) {
+      atomicCAS(a.error, kErrNone, kErrLookback);
+      mbar_wait_bounded(io.val_bar, 0, a.timeout_ns);
+    }
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+      const uint32_t d = packed[i] >> 16;
+      const uint32_t pos = s.warp_cnt[warp][d] + (packed[i] & 0xFFFFu);
+      const int p = wpos + i * kWarp;
+      const uint32_t v = io.val_src == nullptr ? static_cast<uint32_t>(tile_begin + p)
+                                               : ((FULL || p < valid) ? io.val_src[p] : 0u);
+      io.stage_pairs[pos] = make_uint2(static_cast<uint32_t>(keys[i]), v);
+    }
+  } else {
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
     const uint32_t d = packed[i] >> 16;
@@ -345,6 +367,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     __syncthreads();
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) io.stage_vals[packed[i]] = v[i];
+  }
   }
   LSDRS_PHASE(3);  // staging (thread 0's share)
 
@@ -374,12 +397,20 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   for (int i = 0; i < ITEMS; ++i) {
     const int j = i * THREADS + tid;
     if (FULL || j < valid) {
-      const T k = io.stage_keys[j];
+      T k;
+      uint32_t v = 0;
+      if constexpr (kPair64) {
+        const uint2 kv = io.stage_pairs[j];
+        k = static_cast<T>(kv.x);
+        v = kv.y;
+      } else {
+        k = io.stage_keys[j];
+        if constexpr (kVals) v = io.stage_vals[j];
+      }
       const uint32_t d = KeyOp::digit(k, a.shift, a.mask, a.flip);
       const uint32_t g = s.g_off[d] + static_cast<uint32_t>(j);
       kout[g] = k;
       if constexpr (kVals) {
-        const uint32_t v = io.stage_vals[j];
         if (wide)
           vout64[g] = static_cast<int64_t>(static_cast<int32_t>(v));
         else
@@ -411,8 +442,10 @@ struct SweepSmem {
   using T = typename KeyOp::T;
   static constexpr int kTile = THREADS * ITEMS;
   static constexpr bool kVals = VK != kValNone;
-  alignas(128) T keys[kTile];                      // key stage
-  alignas(128) uint32_t vals[kVals ? kTile : 4];   // payloads in, then payload stage
+  static constexpr bool kPair64 = LSDRS_STAGE64 && kVals && sizeof(T) == 4;
+  // key stage, or (key, payload) stage when paired
+  alignas(128) unsigned char stage[kPair64 ? kTile * 8 : kTile * sizeof(T)];
+  alignas(128) uint32_t vals[kVals ? kTile : 4];  // payloads in (then payload stage unpaired)
   TileScratch<THREADS / kWarp, (1 << BITS)> scratch;
   uint64_t bar;
   uint32_t tile_id;
@@ -445,7 +478,8 @@ __global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
   const int64_t off = p.row * a.cols + p.tile_begin;
   TileIo<KeyOp> io;
   io.key_src = static_cast<const T*>(a.keys_in) + off;
-  io.stage_keys = s.keys;
+  io.stage_keys = reinterpret_cast<T*>(s.stage);
+  io.stage_pairs = reinterpret_cast<uint2*>(s.stage);
   io.stage_vals = s.vals;
   io.val_src = nullptr;
   io.val_bar = nullptr;
