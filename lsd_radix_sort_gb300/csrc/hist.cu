@@ -172,22 +172,44 @@ __global__ void __launch_bounds__(kHistThreads, 1) upfront_hist_kernel(HistArgs 
 }
 
 // One CTA per (row, pass): add the slots of the row's chunks, then an
-// exclusive scan over the digits.
-__global__ void __launch_bounds__(kScanThreads) digit_scan_kernel(ScanArgs a) {
+// exclusive scan over the digits.  Q threads share each digit's sum (Q
+// independent partial sums in flight) when the row has many chunks.
+template <int Q>
+__global__ void __launch_bounds__(kScanThreads * Q) digit_scan_kernel(ScanArgs a) {
+  __shared__ uint32_t part[Q][kScanThreads];
   __shared__ uint32_t warp_sums[kScanThreads / kWarp];
   const int tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5;
+  const int d = tid % kScanThreads;  // digit (when < radix)
+  const int q = tid / kScanThreads;  // share of the chunks
   const int64_t row = blockIdx.x / a.passes;
   const int p = blockIdx.x % a.passes;
   const int nb = a.passes * a.radix;
 
-  uint32_t total = 0;
-  if (tid < a.radix) {
+  uint32_t sum = 0;
+  if (d < a.radix) {
     const uint32_t* s = a.slots + row * a.chunks_per_row * static_cast<int64_t>(nb) +
-                        p * a.radix + tid;
-    for (int c = 0; c < a.chunks_per_row; ++c) total += s[static_cast<int64_t>(c) * nb];
+                        p * a.radix + d;
+    int c = q;
+    for (; c + 3 * Q < a.chunks_per_row; c += 4 * Q) {
+      const uint32_t s0 = s[static_cast<int64_t>(c) * nb];
+      const uint32_t s1 = s[static_cast<int64_t>(c + Q) * nb];
+      const uint32_t s2 = s[static_cast<int64_t>(c + 2 * Q) * nb];
+      const uint32_t s3 = s[static_cast<int64_t>(c + 3 * Q) * nb];
+      sum += (s0 + s1) + (s2 + s3);
+    }
+    for (; c < a.chunks_per_row; c += Q) sum += s[static_cast<int64_t>(c) * nb];
   }
-  // block-wide exclusive scan of `total` over tid
+  if (Q > 1) {
+    part[q][d] = sum;
+    __syncthreads();
+    if (q != 0) return;
+    sum = 0;
+#pragma unroll
+    for (int k = 0; k < Q; ++k) sum += part[k][d];
+  }
+  // block-wide exclusive scan of the totals over the first kScanThreads threads
+  const int lane = d & 31, warp = d >> 5;
+  const uint32_t total = sum;
   uint32_t incl = total;
 #pragma unroll
   for (int o = 1; o < kWarp; o <<= 1) {
@@ -195,7 +217,7 @@ __global__ void __launch_bounds__(kScanThreads) digit_scan_kernel(ScanArgs a) {
     if (lane >= o) incl += y;
   }
   if (lane == kWarp - 1) warp_sums[warp] = incl;
-  __syncthreads();
+  asm volatile("bar.sync 1, %0;" ::"n"(kScanThreads));
   if (warp == 0) {
     uint32_t w = lane < kScanThreads / kWarp ? warp_sums[lane] : 0;
     uint32_t wi = w;
@@ -206,10 +228,10 @@ __global__ void __launch_bounds__(kScanThreads) digit_scan_kernel(ScanArgs a) {
     }
     if (lane < kScanThreads / kWarp) warp_sums[lane] = wi - w;
   }
-  __syncthreads();
+  asm volatile("bar.sync 1, %0;" ::"n"(kScanThreads));
   const uint32_t excl = incl - total + warp_sums[warp];
-  if (tid < a.radix) {
-    const int64_t o = (row * a.passes + p) * a.radix + tid;
+  if (d < a.radix) {
+    const int64_t o = (row * a.passes + p) * a.radix + d;
     a.bases[o] = excl;
     if (a.hist_out) a.hist_out[o] = total;
   }
@@ -259,7 +281,10 @@ cudaError_t launch_hist(KeyKind k, int bits, const HistArgs& a, int grid, cudaSt
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s) {
   const int64_t grid = a.rows * a.passes;
-  digit_scan_kernel<<<static_cast<unsigned>(grid), kScanThreads, 0, s>>>(a);
+  if (a.chunks_per_row >= 16)
+    digit_scan_kernel<4><<<static_cast<unsigned>(grid), kScanThreads * 4, 0, s>>>(a);
+  else
+    digit_scan_kernel<1><<<static_cast<unsigned>(grid), kScanThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
