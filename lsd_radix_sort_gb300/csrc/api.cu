@@ -29,7 +29,6 @@ std::vector<ProfRec> g_prof;
 // Runs `launch` bracketed by profiling events when enabled.
 template <class F>
 cudaError_t timed_launch(int kernel, uint64_t units, cudaStream_t s, F&& launch) {
-  g_launches.fetch_add(1, std::memory_order_relaxed);
   ProfRec r{kernel, units, nullptr, nullptr};
   bool prof;
   {
@@ -41,7 +40,9 @@ cudaError_t timed_launch(int kernel, uint64_t units, cudaStream_t s, F&& launch)
       return cudaErrorUnknown;
     cudaEventRecord(r.start, s);
   }
-  cudaError_t e = launch();
+  int launched = 1;
+  cudaError_t e = launch(&launched);
+  g_launches.fetch_add(static_cast<uint64_t>(launched), std::memory_order_relaxed);
   if (prof) {
     cudaEventRecord(r.stop, s);
     std::lock_guard<std::mutex> lk(g_prof_mu);
@@ -155,7 +156,7 @@ rs_status run_front(const Plan& p, const void* keys, uint32_t flip, void* temp,
   h.zero_words = (p.off_status1) / 4;  // header + status0
   const int64_t hgrid = p.rows * p.chunks_per_row;
   const uint64_t n = static_cast<uint64_t>(p.rows) * p.cols;
-  cudaError_t e = timed_launch(0, n, s, [&] {
+  cudaError_t e = timed_launch(0, n, s, [&](int*) {
     return launch_hist(p.key, p.bits, h, static_cast<int>(hgrid), s);
   });
   if (e != cudaSuccess) return RS_ERR_CUDA;
@@ -168,15 +169,15 @@ rs_status run_front(const Plan& p, const void* keys, uint32_t flip, void* temp,
   c.hist_out = hist_out;
   c.bases = bases_out ? bases_out : reinterpret_cast<uint32_t*>(at(temp, p.off_bases));
   e = timed_launch(1, static_cast<uint64_t>(p.rows) * p.passes * p.radix, s,
-                   [&] { return launch_scan(c, s); });
+                   [&](int*) { return launch_scan(c, s); });
   return e == cudaSuccess ? RS_OK : RS_ERR_CUDA;
 }
 
-cudaError_t sweep(const Plan& p, const SweepArgs& a, cudaStream_t s) {
+cudaError_t sweep(const Plan& p, const SweepArgs& a, int* launched, cudaStream_t s) {
   switch (p.key) {
-    case kKeyU32: return launch_sweep_u32(p.val, p.bits, a, p.tiles, s);
-    case kKeyU64: return launch_sweep_u64(p.val, p.bits, a, p.tiles, s);
-    case kKeyF16: return launch_sweep_f16(a, p.tiles, s);
+    case kKeyU32: return launch_sweep_u32(p.val, p.bits, a, launched, s);
+    case kKeyU64: return launch_sweep_u64(p.val, p.bits, a, launched, s);
+    case kKeyF16: return launch_sweep_f16(a, launched, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -250,6 +251,7 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
     a.rows = p.rows;
     a.cols = p.cols;
     a.tiles_per_row = p.tiles_per_row;
+    a.full_per_row = p.cols / p.tile;
     a.shift = p.begin_bit + q * p.bits;
     a.mask = last ? p.last_mask : static_cast<uint32_t>(p.radix - 1);
     a.flip = flip;
@@ -260,7 +262,7 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
     a.tile_counter = header + 1 + q;
     a.error = header;
     a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
-    cudaError_t e = timed_launch(2, n, s, [&] { return sweep(p, a, s); });
+    cudaError_t e = timed_launch(2, n, s, [&](int* k) { return sweep(p, a, k, s); });
     if (e != cudaSuccess) return RS_ERR_CUDA;
     ksrc = a.keys_out;
     vsrc = a.vals_out;
@@ -403,7 +405,7 @@ rs_status rs_lookback_timeout_probe(uint32_t* word, uint64_t timeout_ns, void* s
   if (!word || !result || timeout_ns == 0 || timeout_ns > 10000000000ull) return RS_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(word, 0, 8, s) != cudaSuccess) return RS_ERR_CUDA;
-  cudaError_t e = timed_launch(4, 1, s, [&] {
+  cudaError_t e = timed_launch(4, 1, s, [&](int*) {
     return launch_timeout_probe(word, word + 1, timeout_ns, s);
   });
   if (e != cudaSuccess) return RS_ERR_CUDA;
@@ -422,7 +424,7 @@ rs_status rs_copy_probe(void* dst, const void* src, size_t bytes, void* stream) 
   if (bytes == 0) return RS_OK;
   if (overlap(dst, bytes, src, bytes)) return RS_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = timed_launch(3, bytes, s, [&] { return launch_copy(dst, src, bytes, s); });
+  cudaError_t e = timed_launch(3, bytes, s, [&](int*) { return launch_copy(dst, src, bytes, s); });
   return e == cudaSuccess ? RS_OK : RS_ERR_CUDA;
 }
 

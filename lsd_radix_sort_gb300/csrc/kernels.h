@@ -112,6 +112,7 @@ struct SweepArgs {
   void* vals_out;
   int64_t rows, cols;
   int64_t tiles_per_row;
+  int64_t full_per_row;    // tiles of a row that hold a whole tile of keys
   int shift;
   uint32_t mask;
   uint32_t flip;
@@ -127,11 +128,13 @@ struct SweepArgs {
 
 cudaError_t launch_hist(KeyKind k, int bits, const HistArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
-cudaError_t launch_sweep_u32(ValKind v, int bits, const SweepArgs& a, int64_t grid,
+// One scatter pass: a kernel over the full tiles, then one over each row's
+// partial tile; *launched receives the number of kernels launched (0-2).
+cudaError_t launch_sweep_u32(ValKind v, int bits, const SweepArgs& a, int* launched,
                              cudaStream_t s);
-cudaError_t launch_sweep_u64(ValKind v, int bits, const SweepArgs& a, int64_t grid,
+cudaError_t launch_sweep_u64(ValKind v, int bits, const SweepArgs& a, int* launched,
                              cudaStream_t s);
-cudaError_t launch_sweep_f16(const SweepArgs& a, int64_t grid, cudaStream_t s);
+cudaError_t launch_sweep_f16(const SweepArgs& a, int* launched, cudaStream_t s);
 cudaError_t launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t s);
 cudaError_t launch_timeout_probe(uint32_t* word, uint32_t* error, uint64_t timeout_ns,
                                  cudaStream_t s);

@@ -62,11 +62,6 @@
 #ifndef LSDRS_STATS
 #define LSDRS_STATS 0
 #endif
-// Stage a 4-byte key with its 4-byte payload as one 8-byte word (one
-// scattered shared store per key instead of two).
-#ifndef LSDRS_STAGE64
-#define LSDRS_STAGE64 0
-#endif
 
 namespace lsdrs {
 
@@ -204,16 +199,16 @@ struct TileScratch {
   uint32_t g_off[R];        // output position of staged slot j is g_off[d] + j
 };
 
-// Where a tile's keys and payloads are read from and staged to.  Key and
-// payload sources are warp-striped: the item at tile position p is src[p].
+// Where a tile's keys and payloads are read from and staged to.  The key
+// source is global and the payloads are in shared memory, both by tile
+// position (the item at tile position p is key_src[p], vals[p]).
 template <class KeyOp>
 struct TileIo {
-  const typename KeyOp::T* key_src;  // shared (prefetched) or global
-  const uint32_t* val_src;           // shared, global, or null (generate indices)
+  const typename KeyOp::T* key_src;  // global
   typename KeyOp::T* stage_keys;     // shared, TILE keys
-  uint32_t* stage_vals;              // shared, TILE words (may equal val_src)
-  uint2* stage_pairs;                // shared, TILE (key, payload) words when paired
-  uint64_t* val_bar;                 // completes when a bulk copy filled val_src
+  uint32_t* vals;                    // shared, TILE words: payloads in, then their stage
+  uint64_t* val_bar;                 // non-null: a bulk copy into vals completes on it
+  bool vals_in;                      // payloads were loaded (else indices are generated)
 };
 
 // One tile: rank, publish, look back, stage, write.  Called by every thread
@@ -221,7 +216,7 @@ struct TileIo {
 template <bool FULL, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
 __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
                                            TileScratch<THREADS / kWarp, (1 << BITS)>& s,
-                                           const TileIo<KeyOp>& io, int64_t tile, int64_t row,
+                                           const TileIo<KeyOp>& io, uint32_t* status_row, int64_t row,
                                            int64_t t, int valid) {
   using T = typename KeyOp::T;
   constexpr int R = 1 << BITS;
@@ -235,7 +230,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   const int warp = tid >> 5;
   const int64_t row_base = row * a.cols;
   const int64_t tile_begin = t * TILE;
-  uint32_t* status_tile = a.status + tile * R;
+  uint32_t* status_tile = status_row + t * R;
   const int wpos = warp * WKEYS + lane;  // tile position of item 0
   uint32_t trips = 0, polls = 0;
 #if LSDRS_STATS >= 2
@@ -248,9 +243,12 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     keys[i] = (FULL || wpos + i * kWarp < valid) ? io.key_src[wpos + i * kWarp] : T(0);
 
   // ---- 3. rank within the warp ------------------------------------------
-  // packed[i] = digit << 16 | rank of the item among the warp's keys of
-  // that digit.
-  uint32_t packed[ITEMS];
+  // The rank of item i among the warp's keys of its digit (below
+  // 32 * ITEMS < 2^16) is kept in half i % 2 of packed[i / 2]; the digit
+  // is taken from the key again when it is needed.  Two ranks per register
+  // keep the tile's state in registers.
+  constexpr int NP = (ITEMS + 1) / 2;
+  uint32_t packed[NP];
   uint32_t* wc = s.warp_cnt[warp];
   const uint32_t lt = lanemask_lt();
 #pragma unroll
@@ -268,7 +266,11 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     }
     before = __shfl_sync(kFull, before, leader);
     __syncwarp();
-    packed[i] = (d << 16) | (before + __popc(peers & lt));
+    const uint32_t rank = before + __popc(peers & lt);
+    if (i & 1)
+      packed[i >> 1] |= rank << 16;
+    else
+      packed[i >> 1] = rank;
   }
   __syncthreads();
   LSDRS_PHASE(0);  // loads + ranking
@@ -285,7 +287,8 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     }
     s.tile_start[tid] = sum;
     my_count = (!FULL && tid == R - 1) ? sum - static_cast<uint32_t>(TILE - valid) : sum;
-    st_relaxed(status_tile + tid, (t == 0 ? kFlagP : kFlagA) | my_count);
+    // a partial tile is the last of its row: nothing waits on it
+    if (FULL) st_relaxed(status_tile + tid, (t == 0 ? kFlagP : kFlagA) | my_count);
   }
   __syncthreads();
   LSDRS_PHASE(1);  // warp offsets + publish
@@ -325,28 +328,21 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   LSDRS_PHASE(2);  // digit scan
 
   // ---- 5. stage keys, then payloads, in tile-sorted order ---------------
-  constexpr bool kPair64 = LSDRS_STAGE64 && kVals && sizeof(T) == 4;
-  if constexpr (kPair64) {
-    if (io.val_bar != nullptr && !mbar_wait_bounded(io.val_bar, 0, a.timeout_ns)) {
-      atomicCAS(a.error, kErrNone, kErrLookback);
-      mbar_wait_bounded(io.val_bar, 0, a.timeout_ns);
-    }
-#pragma unroll
-    for (int i = 0; i < ITEMS; ++i) {
-      const uint32_t d = packed[i] >> 16;
-      const uint32_t pos = s.warp_cnt[warp][d] + (packed[i] & 0xFFFFu);
-      const int p = wpos + i * kWarp;
-      const uint32_t v = io.val_src == nullptr ? static_cast<uint32_t>(tile_begin + p)
-                                               : ((FULL || p < valid) ? io.val_src[p] : 0u);
-      io.stage_pairs[pos] = make_uint2(static_cast<uint32_t>(keys[i]), v);
-    }
-  } else {
+  auto half = [](uint32_t w, int i) -> uint32_t { return (i & 1) ? (w >> 16) : (w & 0xFFFFu); };
+  auto item_digit = [&](int i) -> uint32_t {
+    if (!FULL && wpos + i * kWarp >= valid) return R - 1;
+    return KeyOp::digit(opaque(keys[i]), a.shift, a.mask, a.flip);
+  };
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
-    const uint32_t d = packed[i] >> 16;
-    const uint32_t pos = s.warp_cnt[warp][d] + (packed[i] & 0xFFFFu);
+    const uint32_t d = item_digit(i);
+    const uint32_t pos = s.warp_cnt[warp][d] + half(packed[i >> 1], i);
     io.stage_keys[pos] = keys[i];
-    packed[i] = pos;  // keep the staging slot for the payload
+    // keep the staging slot (below TILE < 2^16) for the payload
+    if (i & 1)
+      packed[i >> 1] = (packed[i >> 1] & 0xFFFFu) | (pos << 16);
+    else
+      packed[i >> 1] = (packed[i >> 1] & 0xFFFF0000u) | pos;
   }
   if constexpr (kVals) {
     if (io.val_bar != nullptr && !mbar_wait_bounded(io.val_bar, 0, a.timeout_ns)) {
@@ -355,19 +351,18 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
       atomicCAS(a.error, kErrNone, kErrLookback);
       mbar_wait_bounded(io.val_bar, 0, a.timeout_ns);
     }
-    // The payload source may be the staging buffer itself: read every
-    // thread's payloads before any is overwritten.
+    // The payloads are staged in the buffer they were loaded into: read
+    // every thread's payloads before any is overwritten.
+    const bool vin = VK == kValU32 || io.vals_in;
     uint32_t v[ITEMS];
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
       const int p = wpos + i * kWarp;
-      v[i] = io.val_src == nullptr ? static_cast<uint32_t>(tile_begin + p)
-                                   : ((FULL || p < valid) ? io.val_src[p] : 0u);
+      v[i] = !vin ? static_cast<uint32_t>(tile_begin + p) : ((FULL || p < valid) ? io.vals[p] : 0u);
     }
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < ITEMS; ++i) io.stage_vals[packed[i]] = v[i];
-  }
+    for (int i = 0; i < ITEMS; ++i) io.vals[half(packed[i >> 1], i)] = v[i];
   }
   LSDRS_PHASE(3);  // staging (thread 0's share)
 
@@ -375,8 +370,8 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   if (tid < R) {
     uint32_t excl = 0;
     if (t > 0) {
-      excl = look_back<R, WIN>(a.status + (tile - t) * R + tid, t, a.error, a.timeout_ns, trips, polls);
-      st_relaxed(status_tile + tid, kFlagP | (excl + my_count));
+      excl = look_back<R, WIN>(status_row + tid, t, a.error, a.timeout_ns, trips, polls);
+      if (FULL) st_relaxed(status_tile + tid, kFlagP | (excl + my_count));
     }
     s.g_off[tid] = a.bases[row * a.bases_row_stride + tid] + excl - s.tile_start[tid];
   }
@@ -397,16 +392,9 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   for (int i = 0; i < ITEMS; ++i) {
     const int j = i * THREADS + tid;
     if (FULL || j < valid) {
-      T k;
+      const T k = io.stage_keys[j];
       uint32_t v = 0;
-      if constexpr (kPair64) {
-        const uint2 kv = io.stage_pairs[j];
-        k = static_cast<T>(kv.x);
-        v = kv.y;
-      } else {
-        k = io.stage_keys[j];
-        if constexpr (kVals) v = io.stage_vals[j];
-      }
+      if constexpr (kVals) v = io.vals[j];
       const uint32_t d = KeyOp::digit(k, a.shift, a.mask, a.flip);
       const uint32_t g = s.g_off[d] + static_cast<uint32_t>(j);
       kout[g] = k;
@@ -421,123 +409,155 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   LSDRS_PHASE(6);  // write-out
 }
 
-struct TilePlace {
-  int64_t row, t, tile_begin;
-  int valid;
-};
-
-template <int TILE>
-__device__ __forceinline__ TilePlace place_tile(const SweepArgs& a, int64_t tile) {
-  TilePlace p;
-  p.row = tile / a.tiles_per_row;
-  p.t = tile - p.row * a.tiles_per_row;
-  p.tile_begin = p.t * TILE;
-  p.valid = static_cast<int>(a.cols - p.tile_begin < TILE ? a.cols - p.tile_begin : TILE);
-  return p;
-}
-
-// The grid has one CTA per tile.
+// Shared memory of one tile.
 template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS>
 struct SweepSmem {
   using T = typename KeyOp::T;
   static constexpr int kTile = THREADS * ITEMS;
   static constexpr bool kVals = VK != kValNone;
-  static constexpr bool kPair64 = LSDRS_STAGE64 && kVals && sizeof(T) == 4;
-  // key stage, or (key, payload) stage when paired
-  alignas(128) unsigned char stage[kPair64 ? kTile * 8 : kTile * sizeof(T)];
-  alignas(128) uint32_t vals[kVals ? kTile : 4];  // payloads in (then payload stage unpaired)
+  alignas(128) T stage[kTile];                    // keys in tile-sorted order
+  alignas(128) uint32_t vals[kVals ? kTile : 4];  // payloads in, then their stage
   TileScratch<THREADS / kWarp, (1 << BITS)> scratch;
   uint64_t bar;
   uint32_t tile_id;
   uint32_t abort;
 };
 
-template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB, int WIN>
-__global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
+// One CTA, one tile.  TAIL = false: the full tiles of every row, taken in
+// row-major order from the tile counter.  TAIL = true: the last, partial
+// tile of each row (CTA r takes row r's).  Within a row no tile waits on the
+// partial one, so the tail kernel runs after the full tiles are done; keeping
+// it out of the full-tile kernel leaves that kernel's registers to full tiles.
+template <bool TAIL, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
+__device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
   using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
   using T = typename KeyOp::T;
   constexpr int R = 1 << BITS;
   constexpr int W = THREADS / kWarp;
   constexpr int TILE = S::kTile;
   static_assert(R <= THREADS, "one thread per digit");
-  static_assert(kWarp * ITEMS < 65536, "ranks are packed in 16 bits");
+  static_assert(TILE < 65536, "ranks and staging slots are packed in 16 bits");
 
   extern __shared__ __align__(128) unsigned char smem_raw[];
   S& s = *reinterpret_cast<S*>(smem_raw);
   const int tid = threadIdx.x;
 
   if (tid == 0) {
-    s.tile_id = atomicAdd(a.tile_counter, 1u);
+    s.tile_id = TAIL ? 0u : atomicAdd(a.tile_counter, 1u);
     s.abort = ld_relaxed(a.error) != kErrNone;
   }
   for (int i = tid; i < W * R; i += THREADS) (&s.scratch.warp_cnt[0][0])[i] = 0;
   __syncthreads();
 
-  const int64_t tile = s.tile_id;
-  const TilePlace p = place_tile<TILE>(a, tile);
-  const int64_t off = p.row * a.cols + p.tile_begin;
+  int64_t row, t;
+  if (TAIL) {
+    row = blockIdx.x;
+    t = a.tiles_per_row - 1;
+  } else {
+    // tile ids and tiles per row fit 32 bits (at most 2^30 keys)
+    const uint32_t id = s.tile_id;
+    const uint32_t fpr = static_cast<uint32_t>(a.full_per_row);
+    const uint32_t r32 = id / fpr;
+    row = r32;
+    t = id - r32 * fpr;
+  }
+  // look-back words are indexed by full tile, row-major: row r's tile t at
+  // r * full_per_row + t; partial tiles publish none
+  uint32_t* status_row = a.status + (row * a.full_per_row) * R;
+  const int valid = TAIL ? static_cast<int>(a.cols - t * TILE) : TILE;
+  const int64_t off = row * a.cols + t * TILE;
   TileIo<KeyOp> io;
   io.key_src = static_cast<const T*>(a.keys_in) + off;
-  io.stage_keys = reinterpret_cast<T*>(s.stage);
-  io.stage_pairs = reinterpret_cast<uint2*>(s.stage);
-  io.stage_vals = s.vals;
-  io.val_src = nullptr;
+  io.stage_keys = s.stage;
+  io.vals = s.vals;
   io.val_bar = nullptr;
+  io.vals_in = false;
   if (s.abort) {  // an earlier tile failed: release successors and stop
-    if (tid < R) st_relaxed(a.status + tile * R + tid, kFlagP);
+    if (!TAIL && tid < R) st_relaxed(status_row + t * R + tid, kFlagP);
   } else {
     if (VK != kValNone && a.vals_in != nullptr) {
       // Payloads are not needed before the staging step: a full tile with an
-      // aligned source gets them by one bulk copy issued now; the tile's
+      // aligned source gets them by one bulk copy issued now (the tile's
       // first block-wide barrier orders the barrier's initialisation before
-      // any thread waits on it.
+      // any thread waits on it); otherwise the CTA copies them, and the same
+      // barrier makes them visible.
       const uint32_t* vsrc = static_cast<const uint32_t*>(a.vals_in) + off;
-      io.val_src = vsrc;
-      if (LSDRS_VALS_TMA && p.valid == TILE && (reinterpret_cast<uintptr_t>(vsrc) & 15) == 0) {
+      io.vals_in = true;
+      if (LSDRS_VALS_TMA && !TAIL && (reinterpret_cast<uintptr_t>(vsrc) & 15) == 0) {
         if (tid == 0) {
           mbar_init(&s.bar, 1);
           mbar_arrive_expect_tx(&s.bar, TILE * sizeof(uint32_t));
           bulk_copy_g2s(s.vals, vsrc, TILE * sizeof(uint32_t), &s.bar);
         }
-        io.val_src = s.vals;
         io.val_bar = &s.bar;
+      } else {
+        for (int i = tid; i < valid; i += THREADS) s.vals[i] = ld_stream(vsrc + i);
       }
     }
-    if (p.valid == TILE)
-      sweep_tile<true, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io, tile, p.row, p.t,
-                                                             p.valid);
-    else
-      sweep_tile<false, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io, tile, p.row, p.t,
-                                                              p.valid);
+    sweep_tile<!TAIL, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io, status_row, row, t,
+                                                           valid);
   }
-  if (a.status_zero != nullptr && tid < R) a.status_zero[tile * R + tid] = 0;
+  if (!TAIL && a.status_zero != nullptr && tid < R)
+    a.status_zero[static_cast<int64_t>(s.tile_id) * R + tid] = 0;
 }
 
 template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB, int WIN>
-cudaError_t launch_sweep_t(const SweepArgs& a, int64_t grid, cudaStream_t s) {
-  using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
-  auto kern = onesweep_kernel<KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>;
-  const size_t smem = sizeof(S);
+__global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
+  onesweep_body<false, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a);
+}
+
+template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
+__global__ void __launch_bounds__(THREADS, 1) onesweep_tail_kernel(SweepArgs a) {
+  onesweep_body<true, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a);
+}
+
+template <class K>
+cudaError_t launch_with_smem(K kern, unsigned grid, int threads, size_t smem, cudaStream_t s,
+                             const SweepArgs& a) {
   if (smem > 48 * 1024) {
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  kern<<<static_cast<unsigned>(grid), THREADS, smem, s>>>(a);
+  kern<<<grid, threads, smem, s>>>(a);
   return cudaGetLastError();
 }
 
+// One pass: the full tiles, then the partial tile of each row.  Returns
+// the number of kernels launched in *launched.
+template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB, int WIN>
+cudaError_t launch_sweep_t(const SweepArgs& a, int* launched, cudaStream_t s) {
+  using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
+  constexpr int TILE = S::kTile;
+  const size_t smem = sizeof(S);
+  *launched = 0;
+  const int64_t full = a.rows * a.full_per_row;
+  if (full > 0) {
+    cudaError_t e = launch_with_smem(onesweep_kernel<KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>,
+                                     static_cast<unsigned>(full), THREADS, smem, s, a);
+    if (e != cudaSuccess) return e;
+    ++*launched;
+  }
+  if (a.rows > 0 && a.cols % TILE != 0) {
+    cudaError_t e = launch_with_smem(onesweep_tail_kernel<KeyOp, BITS, VK, THREADS, ITEMS, WIN>,
+                                     static_cast<unsigned>(a.rows), THREADS, smem, s, a);
+    if (e != cudaSuccess) return e;
+    ++*launched;
+  }
+  return cudaSuccess;
+}
+
 template <class KeyOp, int VK, int THREADS, int ITEMS, int MINB, int WIN>
-cudaError_t launch_sweep_bits(int bits, const SweepArgs& a, int64_t grid, cudaStream_t s) {
+cudaError_t launch_sweep_bits(int bits, const SweepArgs& a, int* launched, cudaStream_t s) {
   switch (bits) {
-    case 1: return launch_sweep_t<KeyOp, 1, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
-    case 2: return launch_sweep_t<KeyOp, 2, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
-    case 3: return launch_sweep_t<KeyOp, 3, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
-    case 4: return launch_sweep_t<KeyOp, 4, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
-    case 5: return launch_sweep_t<KeyOp, 5, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
-    case 6: return launch_sweep_t<KeyOp, 6, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
-    case 7: return launch_sweep_t<KeyOp, 7, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
-    case 8: return launch_sweep_t<KeyOp, 8, VK, THREADS, ITEMS, MINB, WIN>(a, grid, s);
+    case 1: return launch_sweep_t<KeyOp, 1, VK, THREADS, ITEMS, MINB, WIN>(a, launched, s);
+    case 2: return launch_sweep_t<KeyOp, 2, VK, THREADS, ITEMS, MINB, WIN>(a, launched, s);
+    case 3: return launch_sweep_t<KeyOp, 3, VK, THREADS, ITEMS, MINB, WIN>(a, launched, s);
+    case 4: return launch_sweep_t<KeyOp, 4, VK, THREADS, ITEMS, MINB, WIN>(a, launched, s);
+    case 5: return launch_sweep_t<KeyOp, 5, VK, THREADS, ITEMS, MINB, WIN>(a, launched, s);
+    case 6: return launch_sweep_t<KeyOp, 6, VK, THREADS, ITEMS, MINB, WIN>(a, launched, s);
+    case 7: return launch_sweep_t<KeyOp, 7, VK, THREADS, ITEMS, MINB, WIN>(a, launched, s);
+    case 8: return launch_sweep_t<KeyOp, 8, VK, THREADS, ITEMS, MINB, WIN>(a, launched, s);
     default: return cudaErrorInvalidValue;
   }
 }
