@@ -18,7 +18,7 @@
 //  3. Rank within the warp: for each item, the lanes holding the same digit
 //     are found by one ballot per digit bit; a lane's rank is the number of
 //     such peers in lower lanes plus the warp's running count of that digit
-//     (a per-warp shared-memory counter that the lowest peer advances).
+//     (a per-warp shared-memory counter that one peer advances).
 //     This is the per-digit exclusive scan of the indicator "digit == d"
 //     (section 13.2's rank within digit), done for all digits at once.
 //  4. A per-digit scan over the warps gives each warp's offset and the
@@ -194,8 +194,8 @@ __device__ __forceinline__ uint32_t look_back(const uint32_t* col, int64_t t, ui
 // Shared-memory arrays every tile needs besides its key/payload buffers.
 template <int W, int R>
 struct TileScratch {
-  uint32_t warp_cnt[W][R];  // per-warp digit counters, then per-warp offsets
-  uint32_t tile_start[R];   // digit counts, then digit starts in the tile
+  alignas(16) uint32_t warp_cnt[W][R];  // per-warp digit counters, then per-warp offsets
+  uint32_t warp_tot[W];     // per-warp sums of the digit-count scan
   uint32_t g_off[R];        // output position of staged slot j is g_off[d] + j
 };
 
@@ -256,15 +256,14 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     uint32_t d = KeyOp::digit(keys[i], a.shift, a.mask, a.flip);
     if (!FULL && wpos + i * kWarp >= valid) d = R - 1;
     const uint32_t peers = digit_peers<BITS>(d);
-    // the highest peer lane advances the counter (one find-leading-bit)
+    // Every peer lane reads the warp's count of its digit (one word per
+    // digit, so a broadcast); after a warp barrier the highest peer lane
+    // (one find-leading-bit) advances it.
+    const uint32_t before = wc[d];
+    __syncwarp();
     uint32_t leader;
     asm("bfind.u32 %0, %1;" : "=r"(leader) : "r"(peers));
-    uint32_t before = 0;
-    if (static_cast<uint32_t>(lane) == leader) {
-      before = wc[d];
-      wc[d] = before + __popc(peers);
-    }
-    before = __shfl_sync(kFull, before, leader);
+    if (static_cast<uint32_t>(lane) == leader) wc[d] = before + __popc(peers);
     __syncwarp();
     const uint32_t rank = before + __popc(peers & lt);
     if (i & 1)
@@ -275,54 +274,45 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   __syncthreads();
   LSDRS_PHASE(0);  // loads + ranking
 
-  // ---- 4. warp offsets, tile counts, publish, digit starts --------------
+  // ---- 4. tile counts, publish, digit starts, warp offsets --------------
+  // Thread d turns the warps' counts of digit d into exclusive prefixes over
+  // the warps and publishes their sum; a block-wide exclusive scan of the
+  // sums gives digit d's start in the tile, which is then added to the
+  // prefixes: warp w's first slot for d (staging reads one word per key;
+  // thread d walks column d, so the column accesses are conflict-free).
   uint32_t my_count = 0;  // this tile's count of digit tid (without padding)
-  if (tid < R) {
-    uint32_t sum = 0;
+  uint32_t start = 0;     // first slot of digit tid in the tile
+  {
+    uint32_t total = 0;
+    if (tid < R) {
 #pragma unroll
-    for (int w = 0; w < W; ++w) {
-      const uint32_t c = s.warp_cnt[w][tid];
-      s.warp_cnt[w][tid] = sum;
-      sum += c;
+      for (int w = 0; w < W; ++w) {
+        const uint32_t c = s.warp_cnt[w][tid];
+        s.warp_cnt[w][tid] = total;
+        total += c;
+      }
+      my_count = (!FULL && tid == R - 1) ? total - static_cast<uint32_t>(TILE - valid) : total;
+      // a partial tile is the last of its row: nothing waits on it
+      if (FULL) st_relaxed(status_tile + tid, (t == 0 ? kFlagP : kFlagA) | my_count);
     }
-    s.tile_start[tid] = sum;
-    my_count = (!FULL && tid == R - 1) ? sum - static_cast<uint32_t>(TILE - valid) : sum;
-    // a partial tile is the last of its row: nothing waits on it
-    if (FULL) st_relaxed(status_tile + tid, (t == 0 ? kFlagP : kFlagA) | my_count);
-  }
-  __syncthreads();
-  LSDRS_PHASE(1);  // warp offsets + publish
-  if (warp == 0) {  // exclusive scan of tile_start over the digits
-    constexpr int PER = (R + kWarp - 1) / kWarp;
-    uint32_t v[PER];
-    uint32_t local = 0;
-#pragma unroll
-    for (int k = 0; k < PER; ++k) {
-      const int d = lane * PER + k;
-      v[k] = d < R ? s.tile_start[d] : 0u;
-      local += v[k];
-    }
-    uint32_t incl = local;
+    uint32_t incl = total;
 #pragma unroll
     for (int o = 1; o < kWarp; o <<= 1) {
       const uint32_t y = __shfl_up_sync(kFull, incl, o);
       if (lane >= o) incl += y;
     }
-    uint32_t run = incl - local;
+    if (lane == kWarp - 1) s.warp_tot[warp] = incl;
+    __syncthreads();
+    LSDRS_PHASE(1);  // counts + publish
+    uint32_t before = 0;
 #pragma unroll
-    for (int k = 0; k < PER; ++k) {
-      const int d = lane * PER + k;
-      if (d < R) s.tile_start[d] = run;
-      run += v[k];
+    for (int w = 0; w + 1 < W; ++w)
+      if (w < warp) before += s.warp_tot[w];
+    start = before + incl - total;
+    if (tid < R) {
+#pragma unroll
+      for (int w = 0; w < W; ++w) s.warp_cnt[w][tid] += start;
     }
-  }
-  __syncthreads();
-  // fold the digit starts into the per-warp offsets: staging then reads one
-  // word per key (conflict-free here: thread d walks column d)
-  if (tid < R) {
-    const uint32_t start = s.tile_start[tid];
-#pragma unroll
-    for (int w = 0; w < W; ++w) s.warp_cnt[w][tid] += start;
   }
   __syncthreads();
   LSDRS_PHASE(2);  // digit scan
@@ -373,7 +363,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
       excl = look_back<R, WIN>(status_row + tid, t, a.error, a.timeout_ns, trips, polls);
       if (FULL) st_relaxed(status_tile + tid, kFlagP | (excl + my_count));
     }
-    s.g_off[tid] = a.bases[row * a.bases_row_stride + tid] + excl - s.tile_start[tid];
+    s.g_off[tid] = a.bases[row * a.bases_row_stride + tid] + excl - start;
   }
   LSDRS_PHASE(4);  // thread 0's look-back
 #if LSDRS_STATS
@@ -446,7 +436,9 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
     s.tile_id = TAIL ? 0u : atomicAdd(a.tile_counter, 1u);
     s.abort = ld_relaxed(a.error) != kErrNone;
   }
-  for (int i = tid; i < W * R; i += THREADS) (&s.scratch.warp_cnt[0][0])[i] = 0;
+  static_assert((W * R) % 4 == 0, "counters are zeroed 16 bytes at a time");
+  for (int i = tid; i < W * R / 4; i += THREADS)
+    reinterpret_cast<uint4*>(&s.scratch.warp_cnt[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
 
   int64_t row, t;
