@@ -53,22 +53,6 @@ __device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// A copy of x the compiler cannot see through: a value derived from it is
-// computed again rather than kept live from an earlier computation on x.
-__device__ __forceinline__ uint32_t opaque(uint32_t x) {
-  asm("mov.b32 %0, %0;" : "+r"(x));
-  return x;
-}
-__device__ __forceinline__ uint64_t opaque(uint64_t x) {
-  asm("mov.b64 %0, %0;" : "+l"(x));
-  return x;
-}
-__device__ __forceinline__ uint16_t opaque(uint16_t x) {
-  uint32_t y = x;
-  asm("mov.b32 %0, %0;" : "+r"(y));
-  return static_cast<uint16_t>(y);
-}
-
 // Streaming loads of data read exactly once per pass.
 template <typename T>
 __device__ __forceinline__ T ld_stream(const T* p) {

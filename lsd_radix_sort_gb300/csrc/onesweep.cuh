@@ -18,7 +18,7 @@
 //  3. Rank within the warp: for each item, the lanes holding the same digit
 //     are found by one ballot per digit bit; a lane's rank is the number of
 //     such peers in lower lanes plus the warp's running count of that digit
-//     (a per-warp shared-memory counter that one peer advances).
+//     (a per-warp shared-memory counter that the peers advance together).
 //     This is the per-digit exclusive scan of the indicator "digit == d"
 //     (section 13.2's rank within digit), done for all digits at once.
 //  4. A per-digit scan over the warps gives each warp's offset and the
@@ -257,13 +257,11 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     if (!FULL && wpos + i * kWarp >= valid) d = R - 1;
     const uint32_t peers = digit_peers<BITS>(d);
     // Every peer lane reads the warp's count of its digit (one word per
-    // digit, so a broadcast); after a warp barrier the highest peer lane
-    // (one find-leading-bit) advances it.
+    // digit, so a broadcast) and, after a warp barrier, stores the advanced
+    // count: the peers write the same value to the same word.
     const uint32_t before = wc[d];
     __syncwarp();
-    uint32_t leader;
-    asm("bfind.u32 %0, %1;" : "=r"(leader) : "r"(peers));
-    if (static_cast<uint32_t>(lane) == leader) wc[d] = before + __popc(peers);
+    wc[d] = before + __popc(peers);
     __syncwarp();
     const uint32_t rank = before + __popc(peers & lt);
     if (i & 1)
@@ -321,18 +319,20 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   auto half = [](uint32_t w, int i) -> uint32_t { return (i & 1) ? (w >> 16) : (w & 0xFFFFu); };
   auto item_digit = [&](int i) -> uint32_t {
     if (!FULL && wpos + i * kWarp >= valid) return R - 1;
-    return KeyOp::digit(opaque(keys[i]), a.shift, a.mask, a.flip);
+    return KeyOp::digit(keys[i], a.shift, a.mask, a.flip);
   };
+  // Two items at a time: their warp offsets are packed like their ranks,
+  // so one add gives both staging slots (each below TILE < 2^16, so the low
+  // half never carries), and packed[] then holds the slots for the payloads.
 #pragma unroll
-  for (int i = 0; i < ITEMS; ++i) {
-    const uint32_t d = item_digit(i);
-    const uint32_t pos = s.warp_cnt[warp][d] + half(packed[i >> 1], i);
-    io.stage_keys[pos] = keys[i];
-    // keep the staging slot (below TILE < 2^16) for the payload
-    if (i & 1)
-      packed[i >> 1] = (packed[i >> 1] & 0xFFFFu) | (pos << 16);
-    else
-      packed[i >> 1] = (packed[i >> 1] & 0xFFFF0000u) | pos;
+  for (int k = 0; k < NP; ++k) {
+    const int i0 = 2 * k, i1 = 2 * k + 1;
+    const uint32_t o0 = s.warp_cnt[warp][item_digit(i0)];
+    const uint32_t o1 = i1 < ITEMS ? s.warp_cnt[warp][item_digit(i1)] : 0u;
+    const uint32_t pos = packed[k] + __byte_perm(o0, o1, 0x5410);
+    io.stage_keys[pos & 0xFFFFu] = keys[i0];
+    if (i1 < ITEMS) io.stage_keys[pos >> 16] = keys[i1];
+    packed[k] = pos;
   }
   if constexpr (kVals) {
     if (io.val_bar != nullptr && !mbar_wait_bounded(io.val_bar, 0, a.timeout_ns)) {
