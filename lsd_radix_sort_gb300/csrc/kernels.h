@@ -28,15 +28,15 @@ struct SweepShape {
 // are the fastest measured on GB300 for 2^28-key sorts.
 #ifndef LSDRS_U32K_T
 #define LSDRS_U32K_T 256
-#define LSDRS_U32K_I 32
-#define LSDRS_U32K_B 3
+#define LSDRS_U32K_I 28
+#define LSDRS_U32K_B 4
 #endif
 #ifndef LSDRS_U32K_W
 #define LSDRS_U32K_W 8
 #endif
 #ifndef LSDRS_U32P_T
 #define LSDRS_U32P_T 256
-#define LSDRS_U32P_I 20
+#define LSDRS_U32P_I 23
 #define LSDRS_U32P_B 4
 #endif
 #ifndef LSDRS_U32P_W
@@ -52,7 +52,7 @@ struct SweepShape {
 #endif
 #ifndef LSDRS_U64P_T
 #define LSDRS_U64P_T 256
-#define LSDRS_U64P_I 16
+#define LSDRS_U64P_I 18
 #define LSDRS_U64P_B 3
 #endif
 #ifndef LSDRS_U64P_W
@@ -113,6 +113,7 @@ struct SweepArgs {
   int64_t rows, cols;
   int64_t tiles_per_row;
   int64_t full_per_row;    // tiles of a row that hold a whole tile of keys
+  int full_tile;           // keys per full tile (set by the pass launcher)
   int shift;
   uint32_t mask;
   uint32_t flip;

@@ -217,7 +217,7 @@ template <bool FULL, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int 
 __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
                                            TileScratch<THREADS / kWarp, (1 << BITS)>& s,
                                            const TileIo<KeyOp>& io, uint32_t* status_row, int64_t row,
-                                           int64_t t, int valid) {
+                                           int64_t t, int64_t tile_begin, int valid) {
   using T = typename KeyOp::T;
   constexpr int R = 1 << BITS;
   constexpr int W = THREADS / kWarp;
@@ -229,7 +229,6 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int64_t row_base = row * a.cols;
-  const int64_t tile_begin = t * TILE;
   uint32_t* status_tile = status_row + t * R;
   const int wpos = warp * WKEYS + lane;  // tile position of item 0
   uint32_t trips = 0, polls = 0;
@@ -441,10 +440,11 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
     reinterpret_cast<uint4*>(&s.scratch.warp_cnt[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
 
-  int64_t row, t;
+  int64_t row, t, tile_begin;
   if (TAIL) {
     row = blockIdx.x;
-    t = a.tiles_per_row - 1;
+    t = a.full_per_row;
+    tile_begin = t * a.full_tile;
   } else {
     // tile ids and tiles per row fit 32 bits (at most 2^30 keys)
     const uint32_t id = s.tile_id;
@@ -452,12 +452,13 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
     const uint32_t r32 = id / fpr;
     row = r32;
     t = id - r32 * fpr;
+    tile_begin = t * TILE;
   }
   // look-back words are indexed by full tile, row-major: row r's tile t at
   // r * full_per_row + t; partial tiles publish none
   uint32_t* status_row = a.status + (row * a.full_per_row) * R;
-  const int valid = TAIL ? static_cast<int>(a.cols - t * TILE) : TILE;
-  const int64_t off = row * a.cols + t * TILE;
+  const int valid = TAIL ? static_cast<int>(a.cols - tile_begin) : TILE;
+  const int64_t off = row * a.cols + tile_begin;
   TileIo<KeyOp> io;
   io.key_src = static_cast<const T*>(a.keys_in) + off;
   io.stage_keys = s.stage;
@@ -487,7 +488,7 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
       }
     }
     sweep_tile<!TAIL, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io, status_row, row, t,
-                                                           valid);
+                                                           tile_begin, valid);
   }
   if (!TAIL && a.status_zero != nullptr && tid < R)
     a.status_zero[static_cast<int64_t>(s.tile_id) * R + tid] = 0;
@@ -515,24 +516,34 @@ cudaError_t launch_with_smem(K kern, unsigned grid, int threads, size_t smem, cu
   return cudaGetLastError();
 }
 
+// The tail kernel runs one CTA per row, alone on the GPU: it takes a wide
+// CTA with few keys per thread, so that one partial tile is ranked by
+// 32 warps instead of 8.
+constexpr int kTailThreads = 1024;
+
 // One pass: the full tiles, then the partial tile of each row.  Returns
 // the number of kernels launched in *launched.
 template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB, int WIN>
-cudaError_t launch_sweep_t(const SweepArgs& a, int* launched, cudaStream_t s) {
+cudaError_t launch_sweep_t(const SweepArgs& args, int* launched, cudaStream_t s) {
   using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
   constexpr int TILE = S::kTile;
-  const size_t smem = sizeof(S);
+  constexpr int TAIL_ITEMS = (TILE + kTailThreads - 1) / kTailThreads;
+  using ST = SweepSmem<KeyOp, BITS, VK, kTailThreads, TAIL_ITEMS>;
+  static_assert(ST::kTile >= TILE, "a tail tile holds any partial tile");
+  SweepArgs a = args;
+  a.full_tile = TILE;
   *launched = 0;
   const int64_t full = a.rows * a.full_per_row;
   if (full > 0) {
     cudaError_t e = launch_with_smem(onesweep_kernel<KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>,
-                                     static_cast<unsigned>(full), THREADS, smem, s, a);
+                                     static_cast<unsigned>(full), THREADS, sizeof(S), s, a);
     if (e != cudaSuccess) return e;
     ++*launched;
   }
   if (a.rows > 0 && a.cols % TILE != 0) {
-    cudaError_t e = launch_with_smem(onesweep_tail_kernel<KeyOp, BITS, VK, THREADS, ITEMS, WIN>,
-                                     static_cast<unsigned>(a.rows), THREADS, smem, s, a);
+    cudaError_t e = launch_with_smem(
+        onesweep_tail_kernel<KeyOp, BITS, VK, kTailThreads, TAIL_ITEMS, WIN>,
+        static_cast<unsigned>(a.rows), kTailThreads, sizeof(ST), s, a);
     if (e != cudaSuccess) return e;
     ++*launched;
   }

@@ -11,7 +11,9 @@ from tests.gpu_util import field, poisoned_like, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
-TILE_U32_KEYS, TILE_U32_PAIRS, TILE_U64, TILE_F16 = 8192, 5120, 4096, 4096
+# tile sizes of the sweep kernels (keys per CTA), so that ragged cases
+# straddle tile boundaries
+TILE_U32_KEYS, TILE_U32_PAIRS, TILE_U64, TILE_U64_PAIRS, TILE_F16 = 7168, 5888, 4096, 4608, 4096
 
 
 def run_keys(rs, keys, begin=0, end=None, bits=8):
@@ -90,7 +92,8 @@ def test_u64_pairs_and_keys(rs, dist, begin, end):
 
 # ---------------------------------------------------- ragged and degenerate
 
-RAGGED = [1, 2, 31, 32, 33, 1000, TILE_U64 - 1, TILE_U64, TILE_U64 + 1, TILE_U32_PAIRS - 1,
+RAGGED = [1, 2, 31, 32, 33, 1000, TILE_U64 - 1, TILE_U64, TILE_U64 + 1, TILE_U64_PAIRS - 1,
+          TILE_U64_PAIRS + 1, TILE_U32_PAIRS - 1,
           TILE_U32_PAIRS + 1, TILE_U32_KEYS - 1, TILE_U32_KEYS, TILE_U32_KEYS + 1,
           3 * TILE_U32_KEYS + 17, 100_003]
 
@@ -107,6 +110,9 @@ def test_ragged_sizes(rs, n):
         assert np.array_equal(run_keys(rs, keys, 0, 32, bits), ek)
     k64 = workloads.u64_uniform(n, 12)
     assert np.array_equal(run_keys(rs, k64, 0, 64, 8), oracle.sort(k64, None, 0, 64, 8)[0])
+    k64o, v64o = run_pairs(rs, k64, vals, 0, 64, 8)
+    e64, ev64 = oracle.sort(k64, vals, 0, 64, 8)
+    assert np.array_equal(k64o, e64) and np.array_equal(v64o, ev64)
 
 
 @pytest.mark.parametrize("bits", [1, 2, 3, 4, 5, 6, 7, 8])
