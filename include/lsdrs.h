@@ -57,6 +57,12 @@ typedef enum rs_status {
 
 typedef enum rs_float_kind { RS_F16 = 0, RS_BF16 = 1 } rs_float_kind;
 
+/* Key types of the typed global sorts. */
+typedef enum rs_key_type {
+  RS_KEY_U32 = 0, RS_KEY_I32 = 1, RS_KEY_F32 = 2,   /* 4-byte keys */
+  RS_KEY_U64 = 3, RS_KEY_I64 = 4, RS_KEY_F64 = 5    /* 8-byte keys */
+} rs_key_type;
+
 /* Largest number of keys in one sort (or one row of a row-wise sort); the
  * device offsets are 32-bit and the bound matches the row limit of the
  * row-wise sort (FlagTree PR #1084: n < 2^30). */
@@ -107,6 +113,34 @@ rs_status radix_sort_pairs_u64(const uint64_t* keys_in, uint64_t* keys_out,
                                const uint32_t* vals_in, uint32_t* vals_out, size_t n,
                                int begin_bit, int end_bit, int digit_bits,
                                void* temp, size_t temp_bytes, void* stream);
+
+/* Typed keys-only sort: stable sort of signed (two's complement), IEEE
+ * float or unsigned keys, ascending or descending.  A radix sort orders bit
+ * patterns, which is the wanted order only for unsigned keys ("100 Days of
+ * GPU", day 35, Pitfalls: sort signed and float keys through a bijection on
+ * the way in).  Keys are ordered by T(k) = k XOR (top bit of k ? neg : pos):
+ * signed keys flip the sign bit; float keys set the sign bit of non-negative
+ * patterns and complement negative ones; descending complements T.  So
+ * -0.0 sorts before +0.0, a NaN with the sign bit clear after +inf and one
+ * with it set before -inf (the order of the bit patterns under T), and
+ * equal keys keep input order in both directions.  T is applied on the fly;
+ * the keys written out are the input bits.
+ *   type       an rs_key_type; 4-byte types take 4-byte keys, 8-byte 8-byte
+ *   descending 0 or 1
+ *   begin_bit, end_bit  the bits of T(k) sorted (all of them: 0 and 8*size)
+ *   temp       scratch of radix_sort_temp_bytes() for the key size
+ * Other arguments and errors as radix_sort_keys_u32; an unknown type or a
+ * descending flag other than 0/1 is RS_ERR_INVALID. */
+rs_status radix_sort_keys_typed(rs_key_type type, int descending, const void* keys_in,
+                                void* keys_out, size_t n, int begin_bit, int end_bit,
+                                int digit_bits, void* temp, size_t temp_bytes, void* stream);
+
+/* Typed key-value sort: radix_sort_keys_typed with a u32 payload, as
+ * radix_sort_pairs_u32. */
+rs_status radix_sort_pairs_typed(rs_key_type type, int descending, const void* keys_in,
+                                 void* keys_out, const uint32_t* vals_in, uint32_t* vals_out,
+                                 size_t n, int begin_bit, int end_bit, int digit_bits,
+                                 void* temp, size_t temp_bytes, void* stream);
 
 /* Scratch size of a row-wise sort of a (rows, cols) 16-bit array. */
 rs_status radix_segmented_sort_temp_bytes(int64_t rows, int64_t cols, size_t* bytes);

@@ -7,8 +7,10 @@ scratch buffer with PyTorch, and passes raw device pointers and the current
 stream to the library.  There is no fallback: if the library is missing or
 fails to load, every call raises.
 
-Keys may be given as 4-byte (uint32/int32) or 8-byte (uint64/int64) tensors;
-their bits are sorted as unsigned integers.  Payloads are 4-byte tensors.
+Keys may be given as 4-byte or 8-byte tensors; by default their bits are
+sorted as unsigned integers, and ``key_type`` ("i32", "f32", "i64", "f64",
+"u32", "u64") with ``descending`` selects the typed sorts.  Payloads are
+4-byte tensors.
 """
 from __future__ import annotations
 
@@ -27,6 +29,8 @@ __all__ = [
 
 RS_OK, RS_ERR_INVALID, RS_ERR_TEMP_TOO_SMALL, RS_ERR_CUDA, RS_ERR_LOOKBACK_TIMEOUT = range(5)
 RS_F16, RS_BF16 = 0, 1
+KEY_TYPES = {"u32": (0, 4), "i32": (1, 4), "f32": (2, 4), "u64": (3, 8), "i64": (4, 8),
+             "f64": (5, 8)}
 RS_MAX_KEYS = (1 << 30) - 1
 KERNEL_NAMES = {0: "upfront_hist", 1: "digit_scan", 2: "onesweep", 3: "copy_probe",
                 4: "timeout_probe"}
@@ -37,7 +41,7 @@ EXPORTED_SYMBOLS = (
     "radix_segmented_sort_f16", "radix_sort_histograms", "radix_sort_device_status",
     "rs_status_string", "rs_set_lookback_timeout_ns", "rs_lookback_timeout_probe",
     "rs_copy_probe", "rs_profile_enable", "rs_profile_read", "rs_launch_count_reset",
-    "radix_sort_pairs_u32_noalloc",
+    "radix_sort_pairs_u32_noalloc", "radix_sort_keys_typed", "radix_sort_pairs_typed",
 )
 
 
@@ -94,6 +98,8 @@ def load_library() -> ctypes.CDLL:
             "rs_copy_probe": [P, P, sz, P],
             "rs_profile_enable": [i],
             "radix_sort_pairs_u32_noalloc": [P, P, P, P, sz, i, i, i, P],
+            "radix_sort_keys_typed": [i, i, P, P, sz, i, i, i, P, sz, P],
+            "radix_sort_pairs_typed": [i, i, P, P, P, P, sz, i, i, i, P, sz, P],
         }
         for name, args in sig.items():
             f = getattr(lib, name)
@@ -173,9 +179,24 @@ def _temp(nbytes: int, device, temp=None):
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
 
+def _key_type(key_type, kb: int, descending: bool):
+    """(type code or None for the unsigned ascending entry points, key bytes)."""
+    if key_type is None:
+        return (None if not descending else (0 if kb == 4 else 3)), kb
+    if key_type not in KEY_TYPES:
+        raise ValueError(f"key_type must be one of {sorted(KEY_TYPES)}")
+    code, size = KEY_TYPES[key_type]
+    if size != kb:
+        raise TypeError(f"key_type {key_type} takes {size}-byte keys, got {kb}-byte")
+    return (None if code in (0, 3) and not descending else code), kb
+
+
 def radix_sort_keys(keys, out=None, begin_bit: int = 0, end_bit: int | None = None,
-                    digit_bits: int = 8, temp=None, stream=None):
-    """Stable ascending sort of the unsigned bits [begin_bit, end_bit) of ``keys``."""
+                    digit_bits: int = 8, temp=None, stream=None, key_type=None,
+                    descending: bool = False):
+    """Stable sort of the bits [begin_bit, end_bit) of ``keys``: unsigned and
+    ascending by default; ``key_type`` and ``descending`` select the typed
+    sort (the bits then belong to the order-preserving transform)."""
     import torch
     lib = load_library()
     keys = keys.reshape(-1)
@@ -186,17 +207,26 @@ def radix_sort_keys(keys, out=None, begin_bit: int = 0, end_bit: int | None = No
         out = torch.empty_like(keys)
     _require_cuda(out)
     n = keys.numel()
+    code, _ = _key_type(key_type, kb, descending)
     tb = temp_bytes(n, kb, 0, begin_bit, end_bit, digit_bits)
     t = _temp(tb, keys.device, temp)
-    f = lib.radix_sort_keys_u32 if kb == 4 else lib.radix_sort_keys_u64
-    _check(f(_ptr(keys), _ptr(out), n, begin_bit, end_bit, digit_bits, _ptr(t),
-             t.numel() * t.element_size(), _stream_ptr(stream)), "radix_sort_keys")
+    tsz = t.numel() * t.element_size()
+    if code is None:
+        f = lib.radix_sort_keys_u32 if kb == 4 else lib.radix_sort_keys_u64
+        st = f(_ptr(keys), _ptr(out), n, begin_bit, end_bit, digit_bits, _ptr(t), tsz,
+               _stream_ptr(stream))
+    else:
+        st = lib.radix_sort_keys_typed(code, int(descending), _ptr(keys), _ptr(out), n, begin_bit,
+                                       end_bit, digit_bits, _ptr(t), tsz, _stream_ptr(stream))
+    _check(st, "radix_sort_keys")
     return out
 
 
 def radix_sort_pairs(keys, values, keys_out=None, values_out=None, begin_bit: int = 0,
-                     end_bit: int | None = None, digit_bits: int = 8, temp=None, stream=None):
-    """Stable key-value sort: 4-byte ``values`` follow their keys."""
+                     end_bit: int | None = None, digit_bits: int = 8, temp=None, stream=None,
+                     key_type=None, descending: bool = False):
+    """Stable key-value sort: 4-byte ``values`` follow their keys (key order
+    as for radix_sort_keys)."""
     import torch
     lib = load_library()
     keys = keys.reshape(-1)
@@ -210,12 +240,19 @@ def radix_sort_pairs(keys, values, keys_out=None, values_out=None, begin_bit: in
     values_out = torch.empty_like(values) if values_out is None else values_out
     _require_cuda(keys_out, values_out)
     n = keys.numel()
+    code, _ = _key_type(key_type, kb, descending)
     tb = temp_bytes(n, kb, 4, begin_bit, end_bit, digit_bits)
     t = _temp(tb, keys.device, temp)
-    f = lib.radix_sort_pairs_u32 if kb == 4 else lib.radix_sort_pairs_u64
-    _check(f(_ptr(keys), _ptr(keys_out), _ptr(values), _ptr(values_out), n, begin_bit, end_bit,
-             digit_bits, _ptr(t), t.numel() * t.element_size(), _stream_ptr(stream)),
-           "radix_sort_pairs")
+    tsz = t.numel() * t.element_size()
+    if code is None:
+        f = lib.radix_sort_pairs_u32 if kb == 4 else lib.radix_sort_pairs_u64
+        st = f(_ptr(keys), _ptr(keys_out), _ptr(values), _ptr(values_out), n, begin_bit, end_bit,
+               digit_bits, _ptr(t), tsz, _stream_ptr(stream))
+    else:
+        st = lib.radix_sort_pairs_typed(code, int(descending), _ptr(keys), _ptr(keys_out),
+                                        _ptr(values), _ptr(values_out), n, begin_bit, end_bit,
+                                        digit_bits, _ptr(t), tsz, _stream_ptr(stream))
+    _check(st, "radix_sort_pairs")
     return keys_out, values_out
 
 

@@ -83,7 +83,7 @@ rs_status make_plan(KeyKind key, ValKind val, int64_t rows, int64_t cols, int be
   Plan p{};
   p.key = key;
   p.val = val;
-  p.key_bytes = key == kKeyU32 ? 4 : key == kKeyU64 ? 8 : 2;
+  p.key_bytes = (key == kKeyU32 || key == kKeyX32) ? 4 : (key == kKeyU64 || key == kKeyX64) ? 8 : 2;
   const int kbits = p.key_bytes * 8;
   if (rows < 0 || cols < 0 || static_cast<uint64_t>(cols) > RS_MAX_KEYS) return RS_ERR_INVALID;
   if (begin_bit < 0 || end_bit > kbits || begin_bit >= end_bit) return RS_ERR_INVALID;
@@ -139,7 +139,7 @@ bool overlap(const void* a, size_t an, const void* b, size_t bn) {
 }
 
 // Enqueue K-HIST and K-SCAN.  hist_out: optional copy of the totals.
-rs_status run_front(const Plan& p, const void* keys, uint32_t flip, void* temp,
+rs_status run_front(const Plan& p, const void* keys, const KeyXform& xf, void* temp,
                     uint32_t* hist_out, uint32_t* bases_out, cudaStream_t s) {
   HistArgs h{};
   h.keys = keys;
@@ -150,7 +150,7 @@ rs_status run_front(const Plan& p, const void* keys, uint32_t flip, void* temp,
   h.begin_bit = p.begin_bit;
   h.passes = p.passes;
   h.last_mask = p.last_mask;
-  h.flip = flip;
+  h.xf = xf;
   h.slots = reinterpret_cast<uint32_t*>(at(temp, p.off_slots));
   h.zero_ptr = reinterpret_cast<uint32_t*>(temp);
   h.zero_words = (p.off_status1) / 4;  // header + status0
@@ -178,6 +178,8 @@ cudaError_t sweep(const Plan& p, const SweepArgs& a, int* launched, cudaStream_t
     case kKeyU32: return launch_sweep_u32(p.val, p.bits, a, launched, s);
     case kKeyU64: return launch_sweep_u64(p.val, p.bits, a, launched, s);
     case kKeyF16: return launch_sweep_f16(a, launched, s);
+    case kKeyX32: return launch_sweep_x32(p.val, p.bits, a, launched, s);
+    case kKeyX64: return launch_sweep_x64(p.val, p.bits, a, launched, s);
   }
   return cudaErrorInvalidValue;
 }
@@ -186,7 +188,7 @@ cudaError_t sweep(const Plan& p, const SweepArgs& a, int* launched, cudaStream_t
 // writes `keys_out` last is chosen by parity so that no copy is needed,
 // except for an in-place sort with an odd number of passes.
 rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const void* vals_in,
-                   void* vals_out, uint32_t flip, void* temp, size_t temp_bytes,
+                   void* vals_out, const KeyXform& xf, void* temp, size_t temp_bytes,
                    cudaStream_t s) {
   const size_t n = static_cast<size_t>(p.rows) * static_cast<size_t>(p.cols);
   if (n == 0) return RS_OK;
@@ -221,7 +223,7 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
       return RS_ERR_INVALID;
   }
 
-  rs_status st = run_front(p, keys_in, flip, temp, nullptr, nullptr, s);
+  rs_status st = run_front(p, keys_in, xf, temp, nullptr, nullptr, s);
   if (st != RS_OK) return st;
 
   uint32_t* header = reinterpret_cast<uint32_t*>(temp);
@@ -254,7 +256,7 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
     a.full_per_row = p.cols / p.tile;
     a.shift = p.begin_bit + q * p.bits;
     a.mask = last ? p.last_mask : static_cast<uint32_t>(p.radix - 1);
-    a.flip = flip;
+    a.xf = xf;
     a.bases = bases + static_cast<size_t>(q) * p.radix;
     a.bases_row_stride = static_cast<int64_t>(p.passes) * p.radix;
     a.status = status[q & 1];
@@ -277,14 +279,41 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
   return RS_OK;
 }
 
-rs_status flat_sort(KeyKind key, ValKind val, const void* ki, void* ko, const void* vi, void* vo,
+rs_status flat_sort(KeyKind key, const KeyXform& xf, ValKind val, const void* ki, void* ko,
+                    const void* vi, void* vo,
                     size_t n, int begin_bit, int end_bit, int bits, void* temp,
                     size_t temp_bytes, void* stream) {
   if (n > RS_MAX_KEYS) return RS_ERR_INVALID;
   Plan p;
   rs_status st = make_plan(key, val, 1, static_cast<int64_t>(n), begin_bit, end_bit, bits, &p);
   if (st != RS_OK) return st;
-  return run_sort(p, ki, ko, vi, vo, 0u, temp, temp_bytes, static_cast<cudaStream_t>(stream));
+  return run_sort(p, ki, ko, vi, vo, xf, temp, temp_bytes, static_cast<cudaStream_t>(stream));
+}
+
+// The key kind and transform of a typed global sort (see keys.cuh): unsigned
+// ascending keys take the identity kernels, everything else the transformed
+// ones.
+bool typed_key(rs_key_type type, int descending, KeyKind* kind, KeyXform* xf) {
+  if (descending != 0 && descending != 1) return false;
+  const bool wide = type == RS_KEY_U64 || type == RS_KEY_I64 || type == RS_KEY_F64;
+  const uint64_t ones = wide ? ~0ull : 0xFFFFFFFFull;
+  const uint64_t sign = wide ? (1ull << 63) : (1ull << 31);
+  uint64_t pos, neg;
+  switch (type) {
+    case RS_KEY_U32: case RS_KEY_U64: pos = neg = 0; break;
+    case RS_KEY_I32: case RS_KEY_I64: pos = neg = sign; break;
+    case RS_KEY_F32: case RS_KEY_F64: pos = sign; neg = ones; break;
+    default: return false;
+  }
+  if (descending) {
+    pos ^= ones;
+    neg ^= ones;
+  }
+  xf->pos = pos;
+  xf->neg = neg;
+  const bool identity = pos == 0 && neg == 0;
+  *kind = wide ? (identity ? kKeyU64 : kKeyX64) : (identity ? kKeyU32 : kKeyX32);
+  return true;
 }
 
 }  // namespace
@@ -307,30 +336,51 @@ rs_status radix_sort_temp_bytes(size_t n, int key_bytes, int value_bytes, int be
 rs_status radix_sort_keys_u32(const uint32_t* keys_in, uint32_t* keys_out, size_t n,
                               int begin_bit, int end_bit, int digit_bits, void* temp,
                               size_t temp_bytes, void* stream) {
-  return flat_sort(kKeyU32, kValNone, keys_in, keys_out, nullptr, nullptr, n, begin_bit, end_bit,
-                   digit_bits, temp, temp_bytes, stream);
+  return flat_sort(kKeyU32, KeyXform{0, 0}, kValNone, keys_in, keys_out, nullptr, nullptr, n,
+                   begin_bit, end_bit, digit_bits, temp, temp_bytes, stream);
 }
 
 rs_status radix_sort_keys_u64(const uint64_t* keys_in, uint64_t* keys_out, size_t n,
                               int begin_bit, int end_bit, int digit_bits, void* temp,
                               size_t temp_bytes, void* stream) {
-  return flat_sort(kKeyU64, kValNone, keys_in, keys_out, nullptr, nullptr, n, begin_bit, end_bit,
-                   digit_bits, temp, temp_bytes, stream);
+  return flat_sort(kKeyU64, KeyXform{0, 0}, kValNone, keys_in, keys_out, nullptr, nullptr, n,
+                   begin_bit, end_bit, digit_bits, temp, temp_bytes, stream);
 }
 
 rs_status radix_sort_pairs_u32(const uint32_t* keys_in, uint32_t* keys_out,
                                const uint32_t* vals_in, uint32_t* vals_out, size_t n,
                                int begin_bit, int end_bit, int digit_bits, void* temp,
                                size_t temp_bytes, void* stream) {
-  return flat_sort(kKeyU32, kValU32, keys_in, keys_out, vals_in, vals_out, n, begin_bit, end_bit,
-                   digit_bits, temp, temp_bytes, stream);
+  return flat_sort(kKeyU32, KeyXform{0, 0}, kValU32, keys_in, keys_out, vals_in, vals_out, n,
+                   begin_bit, end_bit, digit_bits, temp, temp_bytes, stream);
 }
 
 rs_status radix_sort_pairs_u64(const uint64_t* keys_in, uint64_t* keys_out,
                                const uint32_t* vals_in, uint32_t* vals_out, size_t n,
                                int begin_bit, int end_bit, int digit_bits, void* temp,
                                size_t temp_bytes, void* stream) {
-  return flat_sort(kKeyU64, kValU32, keys_in, keys_out, vals_in, vals_out, n, begin_bit, end_bit,
+  return flat_sort(kKeyU64, KeyXform{0, 0}, kValU32, keys_in, keys_out, vals_in, vals_out, n,
+                   begin_bit, end_bit, digit_bits, temp, temp_bytes, stream);
+}
+
+rs_status radix_sort_keys_typed(rs_key_type type, int descending, const void* keys_in,
+                                void* keys_out, size_t n, int begin_bit, int end_bit,
+                                int digit_bits, void* temp, size_t temp_bytes, void* stream) {
+  KeyKind kind;
+  KeyXform xf;
+  if (!typed_key(type, descending, &kind, &xf)) return RS_ERR_INVALID;
+  return flat_sort(kind, xf, kValNone, keys_in, keys_out, nullptr, nullptr, n, begin_bit, end_bit,
+                   digit_bits, temp, temp_bytes, stream);
+}
+
+rs_status radix_sort_pairs_typed(rs_key_type type, int descending, const void* keys_in,
+                                 void* keys_out, const uint32_t* vals_in, uint32_t* vals_out,
+                                 size_t n, int begin_bit, int end_bit, int digit_bits, void* temp,
+                                 size_t temp_bytes, void* stream) {
+  KeyKind kind;
+  KeyXform xf;
+  if (!typed_key(type, descending, &kind, &xf)) return RS_ERR_INVALID;
+  return flat_sort(kind, xf, kValU32, keys_in, keys_out, vals_in, vals_out, n, begin_bit, end_bit,
                    digit_bits, temp, temp_bytes, stream);
 }
 
@@ -352,8 +402,10 @@ rs_status radix_segmented_sort_f16(const uint16_t* in, uint16_t* vals_out, int64
   Plan p;
   rs_status st = make_plan(kKeyF16, kValIdx, rows, cols, 0, 16, 8, &p);
   if (st != RS_OK) return st;
-  return run_sort(p, in, vals_out, nullptr, idx_out, descending ? 0xFFFFu : 0u, temp, temp_bytes,
-                  static_cast<cudaStream_t>(stream));
+  // 16-bit float bijection; descending complements it
+  const uint64_t flip = descending ? 0xFFFFu : 0u;
+  return run_sort(p, in, vals_out, nullptr, idx_out, KeyXform{0x8000u ^ flip, 0xFFFFu ^ flip}, temp,
+                  temp_bytes, static_cast<cudaStream_t>(stream));
 }
 
 rs_status radix_sort_histograms(const void* keys, int key_bytes, size_t n, int begin_bit,
@@ -370,7 +422,8 @@ rs_status radix_sort_histograms(const void* keys, int key_bytes, size_t n, int b
   if (n > 0 && !keys) return RS_ERR_INVALID;
   if (temp_bytes < p.total) return RS_ERR_TEMP_TOO_SMALL;
   if (reinterpret_cast<uintptr_t>(temp) % 256 != 0) return RS_ERR_INVALID;
-  return run_front(p, keys, 0u, temp, hist_out, bases_out, static_cast<cudaStream_t>(stream));
+  return run_front(p, keys, KeyXform{0, 0}, temp, hist_out, bases_out,
+                   static_cast<cudaStream_t>(stream));
 }
 
 rs_status radix_sort_device_status(const void* temp, void* stream) {
@@ -505,6 +558,6 @@ extern "C" rs_status radix_sort_pairs_u32_noalloc(const uint32_t* keys_in, uint3
   }
   // The sort's first kernel zeroes every part of the scratch that must start
   // at zero, so what an earlier call left there does not matter.
-  return run_sort(p, keys_in, keys_out, vals_in, vals_out, 0u, scratch, kNoAllocScratchBytes,
-                  static_cast<cudaStream_t>(stream));
+  return run_sort(p, keys_in, keys_out, vals_in, vals_out, KeyXform{0, 0}, scratch,
+                  kNoAllocScratchBytes, static_cast<cudaStream_t>(stream));
 }

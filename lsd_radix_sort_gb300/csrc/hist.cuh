@@ -1,0 +1,203 @@
+// K-HIST: digit histograms of every pass from one read of the keys.
+//
+// A pass only reorders keys, so the count of each digit of pass p is the
+// same in the unsorted input as in pass p's input; one read of the keys
+// therefore yields the histograms of all passes (FlagTree PR #1084,
+// section 2: "compute_global_hist_kernel" fills a (passes, 2^b) table per
+// row in one sweep).  Counting uses shared-memory counters private to the
+// CTA ("privatized" histograms, CUDA Handbook ch. 16 section 16.3, named in
+// the Radix Sort section as usable without modification), replicated over
+// lane columns so that a warp's increments never serialise on one counter,
+// whatever the key distribution.
+// Each CTA writes its partial counts to its own slot; K-SCAN adds the slots
+// and scans (DSA CUDA from First Principles, section 13.1: the base of digit
+// d is the exclusive prefix sum of the counts of the digits below it).
+#pragma once
+#include "common.cuh"
+#include "kernels.h"
+#include "keys.cuh"
+
+namespace lsdrs {
+
+// Counter columns per digit: lane l counts into column l % kCols.  With 32
+// columns every lane of a warp owns its own column and bank, so a warp's 32
+// increments never collide, whatever the digits are (constant input included).
+// 16 columns when 32 would not fit in shared memory (64-bit keys, 8-bit digits).
+template <class KeyOp, int BITS>
+struct HistCfg {
+  static constexpr int kRadix = 1 << BITS;
+  static constexpr int kMaxPasses = (KeyOp::kBits + BITS - 1) / BITS;
+  static constexpr int kCols =
+      static_cast<size_t>(kMaxPasses) * kRadix * 32 * sizeof(uint32_t) <= 128 * 1024 ? 32 : 16;
+  static constexpr int kVec = 16 / sizeof(typename KeyOp::T);
+  static constexpr int kUnroll = 4;
+  static size_t smem_bytes(int passes) {
+    return static_cast<size_t>(passes) * kRadix * kCols * sizeof(uint32_t);
+  }
+};
+
+// Per-thread view of the counters: shift and mask of every pass held in
+// registers; ALL = every pass of the key type is present (the usual case),
+// which drops the per-pass bound test.
+template <class KeyOp, int BITS, bool ALL>
+struct KeyCounter {
+  using Cfg = HistCfg<KeyOp, BITS>;
+  static constexpr int R = Cfg::kRadix;
+  static constexpr int C = Cfg::kCols;
+  static constexpr int MP = Cfg::kMaxPasses;
+  // many narrow passes (digits of 1-3 bits) would not fit in registers:
+  // those compute shift and mask per key instead
+  static constexpr bool kHeld = MP <= 16;
+  static constexpr int MH = kHeld ? MP : 1;
+  uint32_t* col;
+  int begin_bit, passes;
+  uint32_t last_mask;
+  KeyXform xf;
+  int shift[MH];
+  uint32_t mask[MH];
+
+  __device__ __forceinline__ KeyCounter(uint32_t* c, int b, int np, uint32_t lm,
+                                        const KeyXform& x)
+      : col(c), begin_bit(b), passes(np), last_mask(lm), xf(x) {
+#pragma unroll
+    for (int p = 0; p < MH; ++p) {
+      shift[p] = b + p * BITS;
+      mask[p] = p == np - 1 ? lm : static_cast<uint32_t>(R - 1);
+    }
+  }
+  __device__ __forceinline__ void add(typename KeyOp::T k) const {
+    if constexpr (kHeld) {
+#pragma unroll
+      for (int p = 0; p < MP; ++p) {
+        if (ALL || p < passes) {
+          const uint32_t d = KeyOp::digit(k, shift[p], mask[p], xf);
+          atomicAdd(col + (p * R + d) * C, 1u);
+        }
+      }
+    } else {
+      for (int p = 0; p < passes; ++p) {
+        const uint32_t m = p == passes - 1 ? last_mask : static_cast<uint32_t>(R - 1);
+        const uint32_t d = KeyOp::digit(k, begin_bit + p * BITS, m, xf);
+        atomicAdd(col + (p * R + d) * C, 1u);
+      }
+    }
+  }
+};
+
+// Counts keys [begin, end) of one row slice: a scalar head up to 16-byte
+// alignment, a vectorised body (U 16-byte loads in flight per thread) and a
+// scalar tail.
+template <class KeyOp, int BITS, bool ALL>
+__device__ __forceinline__ void count_range(const typename KeyOp::T* base, int64_t begin,
+                                            int64_t end, const KeyCounter<KeyOp, BITS, ALL>& c) {
+  using T = typename KeyOp::T;
+  using Cfg = HistCfg<KeyOp, BITS>;
+  constexpr int V = Cfg::kVec;
+  constexpr int U = Cfg::kUnroll;
+  const int tid = threadIdx.x;
+  const uintptr_t addr = reinterpret_cast<uintptr_t>(base + begin);
+  int64_t head = static_cast<int64_t>(((16 - (addr & 15)) & 15) / sizeof(T));
+  if (head > end - begin) head = end - begin;
+  const int64_t body_begin = begin + head;
+  const int64_t nvec = (end - body_begin) / V;
+  const int64_t body_end = body_begin + nvec * V;
+  if (tid < head) c.add(base[begin + tid]);
+  if (tid < end - body_end) c.add(base[body_end + tid]);
+  const uint4* vp = reinterpret_cast<const uint4*>(base + body_begin);
+  int64_t v = tid;
+  for (; v + (U - 1) * kHistThreads < nvec; v += U * kHistThreads) {
+    uint4 buf[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) buf[u] = __ldcs(vp + v + u * kHistThreads);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const T* ks = reinterpret_cast<const T*>(&buf[u]);
+#pragma unroll
+      for (int e = 0; e < V; ++e) c.add(ks[e]);
+    }
+  }
+  for (; v < nvec; v += kHistThreads) {
+    uint4 b = __ldcs(vp + v);
+    const T* ks = reinterpret_cast<const T*>(&b);
+#pragma unroll
+    for (int e = 0; e < V; ++e) c.add(ks[e]);
+  }
+}
+
+template <class KeyOp, int BITS>
+__global__ void __launch_bounds__(kHistThreads, 1) upfront_hist_kernel(HistArgs a) {
+  using T = typename KeyOp::T;
+  using Cfg = HistCfg<KeyOp, BITS>;
+  constexpr int R = Cfg::kRadix;
+  constexpr int C = Cfg::kCols;
+  extern __shared__ __align__(16) uint32_t cnt[];
+
+  const int tid = threadIdx.x;
+  const int nb = a.passes * R;
+  for (int i = tid; i < nb * C; i += kHistThreads) cnt[i] = 0;
+
+  // Zero the look-back words and counters the sweeps start from.
+  {
+    const size_t stride = static_cast<size_t>(gridDim.x) * kHistThreads;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * kHistThreads + tid; i < a.zero_words;
+         i += stride)
+      a.zero_ptr[i] = 0;
+  }
+  __syncthreads();
+
+  const int64_t row = blockIdx.x / a.chunks_per_row;
+  const int chunk = blockIdx.x % a.chunks_per_row;
+  const int64_t begin = static_cast<int64_t>(chunk) * a.chunk_len;
+  const int64_t end = begin + a.chunk_len < a.cols ? begin + a.chunk_len : a.cols;
+  const T* base = static_cast<const T*>(a.keys) + row * a.cols;
+  uint32_t* col = cnt + (tid & (C - 1));
+  if (begin < end) {
+    if (a.passes == Cfg::kMaxPasses) {
+      const KeyCounter<KeyOp, BITS, true> c(col, a.begin_bit, a.passes, a.last_mask, a.xf);
+      count_range<KeyOp, BITS, true>(base, begin, end, c);
+    } else {
+      const KeyCounter<KeyOp, BITS, false> c(col, a.begin_bit, a.passes, a.last_mask, a.xf);
+      count_range<KeyOp, BITS, false>(base, begin, end, c);
+    }
+  }
+  __syncthreads();
+
+  uint32_t* slot = a.slots + (row * a.chunks_per_row + chunk) * static_cast<int64_t>(nb);
+  for (int b = tid; b < nb; b += kHistThreads) {
+    uint32_t s = 0;
+#pragma unroll
+    for (int k = 0; k < C; ++k) s += cnt[b * C + (k + b) % C];
+    slot[b] = s;
+  }
+}
+
+template <class KeyOp, int BITS>
+cudaError_t launch_hist_t(const HistArgs& a, int grid, cudaStream_t s) {
+  using Cfg = HistCfg<KeyOp, BITS>;
+  const size_t smem = Cfg::smem_bytes(a.passes);
+  auto kern = upfront_hist_kernel<KeyOp, BITS>;
+  if (smem > 48 * 1024) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  kern<<<grid, kHistThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+template <class KeyOp>
+cudaError_t launch_hist_k(int bits, const HistArgs& a, int grid, cudaStream_t s) {
+  switch (bits) {
+    case 1: return launch_hist_t<KeyOp, 1>(a, grid, s);
+    case 2: return launch_hist_t<KeyOp, 2>(a, grid, s);
+    case 3: return launch_hist_t<KeyOp, 3>(a, grid, s);
+    case 4: return launch_hist_t<KeyOp, 4>(a, grid, s);
+    case 5: return launch_hist_t<KeyOp, 5>(a, grid, s);
+    case 6: return launch_hist_t<KeyOp, 6>(a, grid, s);
+    case 7: return launch_hist_t<KeyOp, 7>(a, grid, s);
+    case 8: return launch_hist_t<KeyOp, 8>(a, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace lsdrs

@@ -7,7 +7,15 @@
 
 namespace lsdrs {
 
-enum KeyKind { kKeyU32 = 0, kKeyU64 = 1, kKeyF16 = 2 };
+// Unsigned ascending keys (u32, u64), any other 32- or 64-bit key (signed,
+// float, or descending: transformed on the fly), and 16-bit float rows.
+enum KeyKind { kKeyU32 = 0, kKeyU64 = 1, kKeyF16 = 2, kKeyX32 = 3, kKeyX64 = 4 };
+
+// The order-preserving map of a key to its unsigned sort key:
+// T(k) = k ^ (top bit of k set ? neg : pos) (see keys.cuh).
+struct KeyXform {
+  uint64_t pos, neg;
+};
 // Payload carried with the keys: none, a u32 array, or a column index that
 // is generated in the first pass, kept as int32 and widened to int64 by the
 // last pass.
@@ -72,8 +80,8 @@ constexpr SweepShape kShapeU64Keys{LSDRS_U64K_T, LSDRS_U64K_I, LSDRS_U64K_B, LSD
 constexpr SweepShape kShapeU64Pairs{LSDRS_U64P_T, LSDRS_U64P_I, LSDRS_U64P_B, LSDRS_U64P_W};
 constexpr SweepShape kShapeF16Idx{LSDRS_F16_T, LSDRS_F16_I, LSDRS_F16_B, LSDRS_F16_W};
 constexpr SweepShape sweep_shape(KeyKind k, ValKind v) {
-  return k == kKeyU32 ? (v == kValNone ? kShapeU32Keys : kShapeU32Pairs)
-       : k == kKeyU64 ? (v == kValNone ? kShapeU64Keys : kShapeU64Pairs)
+  return (k == kKeyU32 || k == kKeyX32) ? (v == kValNone ? kShapeU32Keys : kShapeU32Pairs)
+       : (k == kKeyU64 || k == kKeyX64) ? (v == kValNone ? kShapeU64Keys : kShapeU64Pairs)
                       : kShapeF16Idx;
 }
 
@@ -89,7 +97,7 @@ struct HistArgs {
   int64_t chunk_len;
   int begin_bit, passes;
   uint32_t last_mask;      // digit mask of the last (possibly narrower) pass
-  uint32_t flip;           // 0xFFFF: descending 16-bit float keys
+  KeyXform xf;             // key transform
   uint32_t* slots;         // [rows][chunks_per_row][passes][radix] counts
   uint32_t* zero_ptr;      // words zeroed by the grid before any sweep
   size_t zero_words;
@@ -116,7 +124,7 @@ struct SweepArgs {
   int full_tile;           // keys per full tile (set by the pass launcher)
   int shift;
   uint32_t mask;
-  uint32_t flip;
+  KeyXform xf;             // key transform
   int wide_out;            // kValIdx: write int64 indices
   const uint32_t* bases;   // bases of this pass for row 0
   int64_t bases_row_stride;
@@ -128,12 +136,17 @@ struct SweepArgs {
 };
 
 cudaError_t launch_hist(KeyKind k, int bits, const HistArgs& a, int grid, cudaStream_t s);
+cudaError_t launch_hist_x(KeyKind k, int bits, const HistArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
 // One scatter pass: a kernel over the full tiles, then one over each row's
 // partial tile; *launched receives the number of kernels launched (0-2).
 cudaError_t launch_sweep_u32(ValKind v, int bits, const SweepArgs& a, int* launched,
                              cudaStream_t s);
 cudaError_t launch_sweep_u64(ValKind v, int bits, const SweepArgs& a, int* launched,
+                             cudaStream_t s);
+cudaError_t launch_sweep_x32(ValKind v, int bits, const SweepArgs& a, int* launched,
+                             cudaStream_t s);
+cudaError_t launch_sweep_x64(ValKind v, int bits, const SweepArgs& a, int* launched,
                              cudaStream_t s);
 cudaError_t launch_sweep_f16(const SweepArgs& a, int* launched, cudaStream_t s);
 cudaError_t launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t s);

@@ -1,26 +1,48 @@
 // Key encodings: how a stored key becomes the unsigned integer whose b-bit
 // digits are sorted.
 //
-// Unsigned integers are their own sort key.  16-bit floats (fp16 and bf16
-// share the layout sign|exponent|mantissa) use an order-preserving bijection:
-// a negative pattern is complemented (larger magnitude first), a
-// non-negative one gets its sign bit set (after every negative).  Descending
-// order complements that key, so equal patterns still keep input order.
-// ("100 Days of GPU", day 35, Pitfalls: sort floats through a bijection on
-// the way in; FlagTree PR #1084 folds the descending flag into the key
-// conversion of every load.)  The stored bits are carried unchanged, so no
-// inverse transform is needed on the way out.
+// A radix sort orders bit patterns, which is the wanted order only for
+// unsigned integers ("100 Days of GPU", day 35, Pitfalls: negatives come
+// after positives and negative floats come out backwards; the fix is a
+// bijection on the way in).  The bijection used here is
+//     T(k) = k XOR (top bit of k set ? neg : pos)
+// with two constants per key type (width w, sign bit s = 1 << (w-1)):
+//     unsigned        pos = neg = 0
+//     two's-complement pos = neg = s          (flip the sign bit)
+//     IEEE float      pos = s, neg = all ones (non-negative: set the sign
+//                                              bit; negative: complement)
+// and descending order complements T (pos and neg complemented), so that
+// equal patterns still keep input order.  fp16 and bf16 share the float
+// layout (FlagTree PR #1084 folds the descending flag into the key
+// conversion of every load).  T is applied on the fly at every digit
+// extraction and never stored: the stored bits are carried unchanged, so no
+// inverse is needed on the way out.
 #pragma once
 #include <cstdint>
 
+#include "kernels.h"
+
 namespace lsdrs {
 
+// Unsigned 32-bit keys in ascending order: T is the identity.
 struct KeyU32 {
   using T = uint32_t;
   static constexpr int kBits = 32;
   __device__ __forceinline__ static uint32_t digit(T k, int shift, uint32_t mask,
-                                                   uint32_t /*flip*/) {
+                                                   const KeyXform&) {
     return (k >> shift) & mask;
+  }
+};
+
+// Any other 32-bit key: signed or float, or descending.
+struct KeyX32 {
+  using T = uint32_t;
+  static constexpr int kBits = 32;
+  __device__ __forceinline__ static uint32_t digit(T k, int shift, uint32_t mask,
+                                                   const KeyXform& x) {
+    const uint32_t t = k ^ (static_cast<int32_t>(k) < 0 ? static_cast<uint32_t>(x.neg)
+                                                        : static_cast<uint32_t>(x.pos));
+    return (t >> shift) & mask;
   }
 };
 
@@ -28,23 +50,31 @@ struct KeyU64 {
   using T = uint64_t;
   static constexpr int kBits = 64;
   __device__ __forceinline__ static uint32_t digit(T k, int shift, uint32_t mask,
-                                                   uint32_t /*flip*/) {
+                                                   const KeyXform&) {
     return static_cast<uint32_t>(k >> shift) & mask;
   }
 };
 
-// 16-bit float patterns; flip = 0xFFFF for descending, 0 for ascending.
+struct KeyX64 {
+  using T = uint64_t;
+  static constexpr int kBits = 64;
+  __device__ __forceinline__ static uint32_t digit(T k, int shift, uint32_t mask,
+                                                   const KeyXform& x) {
+    const uint64_t t = k ^ (static_cast<int64_t>(k) < 0 ? x.neg : x.pos);
+    return static_cast<uint32_t>(t >> shift) & mask;
+  }
+};
+
+// 16-bit float keys (fp16 / bf16 bit patterns).
 struct KeyF16Bits {
   using T = uint16_t;
   static constexpr int kBits = 16;
-  __device__ __forceinline__ static uint32_t order_key(T u, uint32_t flip) {
-    uint32_t x = u;
-    uint32_t t = (x & 0x8000u) ? (~x & 0xFFFFu) : (x | 0x8000u);
-    return t ^ flip;
-  }
   __device__ __forceinline__ static uint32_t digit(T k, int shift, uint32_t mask,
-                                                   uint32_t flip) {
-    return (order_key(k, flip) >> shift) & mask;
+                                                   const KeyXform& x) {
+    const uint32_t u = k;
+    const uint32_t t = u ^ ((u & 0x8000u) ? static_cast<uint32_t>(x.neg)
+                                          : static_cast<uint32_t>(x.pos));
+    return (t >> shift) & mask;
   }
 };
 

@@ -216,8 +216,9 @@ struct TileIo {
 template <bool FULL, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
 __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
                                            TileScratch<THREADS / kWarp, (1 << BITS)>& s,
-                                           const TileIo<KeyOp>& io, uint32_t* status_row, int64_t row,
-                                           int64_t t, int64_t tile_begin, int valid) {
+                                           const TileIo<KeyOp>& io, uint32_t* status_row,
+                                           int64_t row, int64_t t, int64_t tile_begin,
+                                           int valid) {
   using T = typename KeyOp::T;
   constexpr int R = 1 << BITS;
   constexpr int W = THREADS / kWarp;
@@ -252,7 +253,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   const uint32_t lt = lanemask_lt();
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
-    uint32_t d = KeyOp::digit(keys[i], a.shift, a.mask, a.flip);
+    uint32_t d = KeyOp::digit(keys[i], a.shift, a.mask, a.xf);
     if (!FULL && wpos + i * kWarp >= valid) d = R - 1;
     const uint32_t peers = digit_peers<BITS>(d);
     // Every peer lane reads the warp's count of its digit (one word per
@@ -318,7 +319,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   auto half = [](uint32_t w, int i) -> uint32_t { return (i & 1) ? (w >> 16) : (w & 0xFFFFu); };
   auto item_digit = [&](int i) -> uint32_t {
     if (!FULL && wpos + i * kWarp >= valid) return R - 1;
-    return KeyOp::digit(keys[i], a.shift, a.mask, a.flip);
+    return KeyOp::digit(keys[i], a.shift, a.mask, a.xf);
   };
   // Two items at a time: their warp offsets are packed like their ranks,
   // so one add gives both staging slots (each below TILE < 2^16, so the low
@@ -384,7 +385,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
       const T k = io.stage_keys[j];
       uint32_t v = 0;
       if constexpr (kVals) v = io.vals[j];
-      const uint32_t d = KeyOp::digit(k, a.shift, a.mask, a.flip);
+      const uint32_t d = KeyOp::digit(k, a.shift, a.mask, a.xf);
       const uint32_t g = s.g_off[d] + static_cast<uint32_t>(j);
       kout[g] = k;
       if constexpr (kVals) {

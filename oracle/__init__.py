@@ -79,6 +79,13 @@ def _load():
             f.argtypes = [P, sz, i, i, i, P]
             f.restype = i
         lib.or_order_key16.argtypes = [ctypes.c_uint16, i]
+        lib.or_order_key32.argtypes = [ctypes.c_uint32, i, i]
+        lib.or_order_key32.restype = ctypes.c_uint32
+        lib.or_order_key64.argtypes = [ctypes.c_uint64, i, i]
+        lib.or_order_key64.restype = ctypes.c_uint64
+        for name in ("or_sort_typed32", "or_sort_typed64"):
+            f = getattr(lib, name)
+            f.argtypes = [P, P, P, P, sz, i, i, i, i, i]
         lib.or_order_key16.restype = ctypes.c_uint16
         lib.or_segmented_sort16.argtypes = [P, P, P, i64, i64, i]
         lib.or_segmented_sort16.restype = i
@@ -169,6 +176,45 @@ def pass_histograms(keys: np.ndarray, begin_bit: int = 0, end_bit: int | None = 
     _check(f(_ptr(keys), keys.size, begin_bit, end_bit, digit_bits, _ptr(hist)),
            "pass_histograms")
     return hist[:p]
+
+
+_TYPES = {"u32": (0, 4), "i32": (1, 4), "f32": (2, 4), "u64": (0, 8), "i64": (1, 8),
+          "f64": (2, 8)}
+
+
+def order_key(bits: int, key_type: str, descending: bool = False) -> int:
+    """T(k) of one 32/64-bit pattern under the typed bijection."""
+    code, size = _TYPES[key_type]
+    lib = _load()
+    f = lib.or_order_key32 if size == 4 else lib.or_order_key64
+    return int(f(bits & ((1 << (8 * size)) - 1), code, int(bool(descending))))
+
+
+def sort_typed(keys: np.ndarray, key_type: str, values: np.ndarray | None = None,
+               descending: bool = False, begin_bit: int = 0, end_bit: int | None = None,
+               digit_bits: int = 8):
+    """Stable sort of typed keys (any 4- or 8-byte dtype, read as bit
+    patterns) by the bits [begin_bit, end_bit) of T(k).  Returns
+    (keys_out in the input dtype, values_out)."""
+    code, size = _TYPES[key_type]
+    keys = np.ascontiguousarray(keys)
+    if keys.dtype.itemsize != size:
+        raise TypeError(f"{key_type} keys are {size}-byte, got {keys.dtype}")
+    bits_t = np.uint32 if size == 4 else np.uint64
+    kin = keys.view(bits_t)
+    lib = _load()
+    f = lib.or_sort_typed32 if size == 4 else lib.or_sort_typed64
+    end_bit = 8 * size if end_bit is None else end_bit
+    kout = np.empty_like(kin)
+    vout = None
+    if values is not None:
+        values = np.ascontiguousarray(values, dtype=np.uint32)
+        if values.size != kin.size:
+            raise ValueError("values must have one entry per key")
+        vout = np.empty_like(values)
+    _check(f(_ptr(kin), _ptr(kout), _ptr(values), _ptr(vout), kin.size, code,
+             int(bool(descending)), begin_bit, end_bit, digit_bits), "sort_typed")
+    return kout.view(keys.dtype), vout
 
 
 def order_key16(bits: int, descending: bool = False) -> int:

@@ -34,6 +34,12 @@
  *    whose unsigned order is the float order (100 Days of GPU, day 35,
  *    "Pitfalls": a bijection on the way in); descending order sorts ~T(u)
  *    ascending, so ties keep input order in both directions.
+ *  - Typed 32/64-bit keys follow the same plain reading of that passage:
+ *    two's-complement keys flip the sign bit; IEEE floats complement
+ *    negative patterns and set the sign bit of non-negative ones (the
+ *    16-bit rule at full width); descending complements the result.  -0.0
+ *    and +0.0, and NaNs of either sign, are ordered by their patterns under
+ *    that map (the page gives no other rule).
  */
 #include <stdint.h>
 #include <stdlib.h>
@@ -281,3 +287,63 @@ int or_segmented_histograms16(const uint16_t *in, int64_t rows, int64_t cols,
   free(digit);
   return OR_OK;
 }
+
+/* ---- typed 32/64-bit keys: bijection to unsigned order, then the sort ---- */
+
+enum { OR_UNSIGNED = 0, OR_SIGNED = 1, OR_FLOAT = 2 };
+
+/* T(k) for a key of `type`: unsigned keys are their own order; signed keys
+ * flip the sign bit (two's complement order -> unsigned order); floats
+ * complement negative patterns (larger magnitudes first) and set the sign
+ * bit of the others.  Descending complements T. */
+uint32_t or_order_key32(uint32_t k, int type, int descending) {
+  const uint32_t sign = 0x80000000u;
+  uint32_t t = k;
+  if (type == OR_SIGNED) t = k ^ sign;
+  if (type == OR_FLOAT) t = (k & sign) ? ~k : (k | sign);
+  return descending ? ~t : t;
+}
+
+uint64_t or_order_key64(uint64_t k, int type, int descending) {
+  const uint64_t sign = 0x8000000000000000ull;
+  uint64_t t = k;
+  if (type == OR_SIGNED) t = k ^ sign;
+  if (type == OR_FLOAT) t = (k & sign) ? ~k : (k | sign);
+  return descending ? ~t : t;
+}
+
+/* Stable sort of typed keys on bits [begin_bit, end_bit) of T(k): sort T(k)
+ * with each key's input position as payload, then gather the original keys
+ * (and payloads) in that order. */
+#define OR_DEFINE_TYPED(NAME, KEY_T, ORDER, SORT)                              \
+  int NAME(const KEY_T *keys_in, KEY_T *keys_out, const uint32_t *vals_in,     \
+           uint32_t *vals_out, size_t n, int type, int descending,             \
+           int begin_bit, int end_bit, int b) {                                \
+    if (type < OR_UNSIGNED || type > OR_FLOAT) return OR_ERR_INVALID;          \
+    if (descending != 0 && descending != 1) return OR_ERR_INVALID;             \
+    if (n == 0) return SORT(keys_in, keys_out, NULL, NULL, 0, begin_bit,       \
+                            end_bit, b);                                       \
+    KEY_T *t = (KEY_T *)malloc(sizeof(KEY_T) * n);                             \
+    KEY_T *ts = (KEY_T *)malloc(sizeof(KEY_T) * n);                            \
+    uint32_t *pos = (uint32_t *)malloc(4 * n);                                 \
+    uint32_t *order = (uint32_t *)malloc(4 * n);                               \
+    int rc = OR_ERR_NOMEM;                                                     \
+    if (t && ts && pos && order) {                                             \
+      for (size_t i = 0; i < n; i++) {                                         \
+        t[i] = ORDER(keys_in[i], type, descending);                            \
+        pos[i] = (uint32_t)i;                                                  \
+      }                                                                        \
+      rc = SORT(t, ts, pos, order, n, begin_bit, end_bit, b);                  \
+      if (rc == OR_OK) {                                                       \
+        for (size_t i = 0; i < n; i++) {                                       \
+          keys_out[i] = keys_in[order[i]];                                     \
+          if (vals_in) vals_out[i] = vals_in[order[i]];                        \
+        }                                                                      \
+      }                                                                        \
+    }                                                                          \
+    free(t); free(ts); free(pos); free(order);                                 \
+    return rc;                                                                 \
+  }
+
+OR_DEFINE_TYPED(or_sort_typed32, uint32_t, or_order_key32, or_sort_u32)
+OR_DEFINE_TYPED(or_sort_typed64, uint64_t, or_order_key64, or_sort_u64)

@@ -103,6 +103,16 @@ def test_sort_calls_validate_before_launch(lib):
     assert lib.radix_segmented_sort_f16(bogus, bogus, bogus, 2, 2, 0, 2, temp, big, None) == 1
     assert lib.radix_segmented_sort_f16(bogus, bogus, bogus, -1, 2, 0, 0, temp, big, None) == 1
     assert lib.radix_segmented_sort_f16(bogus, bogus, bogus, 0, 5, 0, 0, temp, big, None) == 0
+    # typed sorts: unknown key type, bad descending flag, bad bit range, n == 0
+    assert lib.radix_sort_keys_typed(9, 0, bogus, bogus, 100, 0, 32, 8, temp, big, None) == 1
+    assert lib.radix_sort_keys_typed(-1, 0, bogus, bogus, 100, 0, 32, 8, temp, big, None) == 1
+    assert lib.radix_sort_keys_typed(1, 2, bogus, bogus, 100, 0, 32, 8, temp, big, None) == 1
+    assert lib.radix_sort_keys_typed(2, 0, bogus, bogus, 100, 0, 33, 8, temp, big, None) == 1
+    assert lib.radix_sort_pairs_typed(5, 1, bogus, bogus, bogus, bogus, 100, 0, 65, 8, temp, big,
+                                      None) == 1
+    assert lib.radix_sort_pairs_typed(4, 0, bogus, bogus, None, None, 100, 0, 64, 8, temp, big,
+                                      None) == 1
+    assert lib.radix_sort_keys_typed(2, 1, None, None, 0, 0, 32, 8, None, 0, None) == 0
     # histograms: bad key width
     assert lib.radix_sort_histograms(bogus, 2, 100, 0, 16, 8, bogus, bogus, temp, big, None) == 1
     # copy probe: misaligned sizes
