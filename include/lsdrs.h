@@ -186,6 +186,23 @@ rs_status radix_sort_histograms(const void* keys, int key_bytes, size_t n,
 rs_status radix_sort_device_status(const void* temp, void* stream);
 
 /* Human-readable name of a status code (static storage). */
+/* Pass skipping, for every sort enqueued after the call (process-wide;
+ * default off).  With it on, a pass in which every key (every key of every
+ * row, for a row-wise sort) has the same digit is the identity permutation
+ * and is not run: the decision is taken on the device from the upfront
+ * histograms, so nothing waits for it, and the output is the same.  A sort
+ * of keys that vary in every digit pays about 1% for the device-side
+ * schedule, which is why it is off by default.
+ *   on   0 or 1 (anything else: RS_ERR_INVALID) */
+rs_status rs_set_pass_skipping(int on);
+
+/* Passes run by the last sort enqueued with this scratch buffer (all of
+ * them unless pass skipping is on).  Synchronises `stream` and reads the
+ * count.
+ *   temp    (device) the scratch buffer of that sort
+ *   passes  (host) receives the count (0 .. passes of the bit range) */
+rs_status radix_sort_passes_run(const void* temp, int* passes, void* stream);
+
 const char* rs_status_string(rs_status status);
 
 /* Limit in nanoseconds on one look-back wait inside the scatter kernels

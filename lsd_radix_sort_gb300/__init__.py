@@ -23,7 +23,7 @@ from . import build as _build
 __all__ = [
     "RadixSortError", "load_library", "library_path", "temp_bytes", "radix_sort_keys",
     "radix_sort_pairs", "segmented_sort", "segmented_temp_bytes", "upfront_histograms",
-    "device_status", "copy_probe", "set_lookback_timeout_ns", "lookback_timeout_probe",
+    "device_status", "passes_run", "set_pass_skipping", "copy_probe", "set_lookback_timeout_ns", "lookback_timeout_probe",
     "profile_enable", "profile_read", "launch_count_reset", "EXPORTED_SYMBOLS",
 ]
 
@@ -33,7 +33,7 @@ KEY_TYPES = {"u32": (0, 4), "i32": (1, 4), "f32": (2, 4), "u64": (3, 8), "i64": 
              "f64": (5, 8)}
 RS_MAX_KEYS = (1 << 30) - 1
 KERNEL_NAMES = {0: "upfront_hist", 1: "digit_scan", 2: "onesweep", 3: "copy_probe",
-                4: "timeout_probe"}
+                4: "timeout_probe", 5: "finish"}
 
 EXPORTED_SYMBOLS = (
     "radix_sort_temp_bytes", "radix_sort_keys_u32", "radix_sort_keys_u64",
@@ -42,6 +42,7 @@ EXPORTED_SYMBOLS = (
     "rs_status_string", "rs_set_lookback_timeout_ns", "rs_lookback_timeout_probe",
     "rs_copy_probe", "rs_profile_enable", "rs_profile_read", "rs_launch_count_reset",
     "radix_sort_pairs_u32_noalloc", "radix_sort_keys_typed", "radix_sort_pairs_typed",
+    "radix_sort_passes_run", "rs_set_pass_skipping",
 )
 
 
@@ -99,6 +100,8 @@ def load_library() -> ctypes.CDLL:
             "rs_profile_enable": [i],
             "radix_sort_pairs_u32_noalloc": [P, P, P, P, sz, i, i, i, P],
             "radix_sort_keys_typed": [i, i, P, P, sz, i, i, i, P, sz, P],
+            "radix_sort_passes_run": [P, P, P],
+            "rs_set_pass_skipping": [i],
             "radix_sort_pairs_typed": [i, i, P, P, P, P, sz, i, i, i, P, sz, P],
         }
         for name, args in sig.items():
@@ -306,6 +309,21 @@ def upfront_histograms(keys, begin_bit: int = 0, end_bit: int | None = None,
                                      t.numel() * t.element_size(), _stream_ptr(stream)),
            "radix_sort_histograms")
     return hist[:passes], bases[:passes]
+
+
+def set_pass_skipping(on: bool):
+    """Skip identity passes (every key with the same digit) from now on
+    (process-wide; off by default)."""
+    _check(load_library().rs_set_pass_skipping(int(bool(on))), "rs_set_pass_skipping")
+
+
+def passes_run(temp, stream=None) -> int:
+    """Passes the last sort with this scratch buffer ran (identity passes,
+    where every key has the same digit, are skipped).  Synchronises."""
+    out = ctypes.c_int(0)
+    _check(load_library().radix_sort_passes_run(_ptr(temp), ctypes.byref(out), _stream_ptr(stream)),
+           "radix_sort_passes_run")
+    return out.value
 
 
 def device_status(temp, stream=None) -> int:

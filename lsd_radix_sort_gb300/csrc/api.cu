@@ -15,6 +15,7 @@ namespace {
 
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_pass_skipping{0};
 
 // ---------------------------------------------------------------- profiling
 struct ProfRec {
@@ -53,7 +54,7 @@ cudaError_t timed_launch(int kernel, uint64_t units, cudaStream_t s, F&& launch)
 
 // -------------------------------------------------------------------- plan
 // Scratch layout (offsets in bytes from `temp`, each 256-byte aligned):
-//   header   : word 0 = device error word, words 1..64 = tile counters
+//   header   : device error word, tile counters, pass schedule (kernels.h)
 //   status0  : look-back words of even passes  [tiles][radix] u32
 //   status1  : look-back words of odd passes   [tiles][radix] u32
 //   bases    : [rows][passes][radix] u32
@@ -61,8 +62,8 @@ cudaError_t timed_launch(int kernel, uint64_t units, cudaStream_t s, F&& launch)
 //   alt_keys : ping-pong key buffer
 //   alt_vals : ping-pong payload buffer (u32 / int32 indices)
 // header and status0 are contiguous: K-HIST zeroes them in one range.
-constexpr size_t kHeaderBytes = 512;
-constexpr int kMaxPasses = 64;
+constexpr size_t kHeaderBytes = 1024;
+static_assert((kHdrNontrivial + kMaxPasses) * 4 <= kHeaderBytes, "header layout");
 
 struct Plan {
   KeyKind key;
@@ -101,6 +102,7 @@ rs_status make_plan(KeyKind key, ValKind val, int64_t rows, int64_t cols, int be
   p.tile = sweep_shape(key, val).tile();
   p.tiles_per_row = (cols + p.tile - 1) / p.tile;
   p.tiles = rows * p.tiles_per_row;
+  if (p.tiles > static_cast<int64_t>(kTileMask)) return RS_ERR_INVALID;  // tile ids: 24 bits
   // K-HIST chunking: enough CTAs to fill the GPU, at least kHistMinChunk keys each.
   int64_t want = rows > 0 ? (kHistTargetCtas + rows - 1) / rows : 1;
   int64_t max_chunks = (cols + kHistMinChunk - 1) / kHistMinChunk;
@@ -140,7 +142,8 @@ bool overlap(const void* a, size_t an, const void* b, size_t bn) {
 
 // Enqueue K-HIST and K-SCAN.  hist_out: optional copy of the totals.
 rs_status run_front(const Plan& p, const void* keys, const KeyXform& xf, void* temp,
-                    uint32_t* hist_out, uint32_t* bases_out, cudaStream_t s) {
+                    uint32_t* hist_out, uint32_t* bases_out, bool in_place, bool dynamic,
+                    cudaStream_t s) {
   HistArgs h{};
   h.keys = keys;
   h.rows = p.rows;
@@ -168,6 +171,10 @@ rs_status run_front(const Plan& p, const void* keys, const KeyXform& xf, void* t
   c.radix = p.radix;
   c.hist_out = hist_out;
   c.bases = bases_out ? bases_out : reinterpret_cast<uint32_t*>(at(temp, p.off_bases));
+  c.header = reinterpret_cast<uint32_t*>(temp);
+  c.cols = p.cols;
+  c.in_place = in_place ? 1 : 0;
+  c.dynamic = dynamic ? 1 : 0;
   e = timed_launch(1, static_cast<uint64_t>(p.rows) * p.passes * p.radix, s,
                    [&](int*) { return launch_scan(c, s); });
   return e == cudaSuccess ? RS_OK : RS_ERR_CUDA;
@@ -223,58 +230,83 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
       return RS_ERR_INVALID;
   }
 
-  rs_status st = run_front(p, keys_in, xf, temp, nullptr, nullptr, s);
+  if (p.val == kValIdx && p.passes > 2) return RS_ERR_INVALID;  // 16-bit keys: two passes
+
+  const bool dynamic = g_pass_skipping.load(std::memory_order_relaxed) != 0;
+  rs_status st = run_front(p, keys_in, xf, temp, nullptr, nullptr, in_place, dynamic, s);
   if (st != RS_OK) return st;
 
+  // With pass skipping, K-SCAN has written the schedule (which passes run,
+  // from which buffer to which) and every pass is launched, a skipped one
+  // returning at once.  Otherwise every pass runs on the host's schedule.
   uint32_t* header = reinterpret_cast<uint32_t*>(temp);
-  uint32_t* status[2] = {reinterpret_cast<uint32_t*>(at(temp, p.off_status0)),
-                         reinterpret_cast<uint32_t*>(at(temp, p.off_status1))};
   void* alt_keys = at(temp, p.off_alt_keys);
   void* alt_vals = at(temp, p.off_alt_vals);
   const uint32_t* bases = reinterpret_cast<const uint32_t*>(at(temp, p.off_bases));
-  // kValIdx: the int32 indices live only in alt_vals; the last pass widens.
-  const bool odd_copy = in_place && (p.passes % 2 == 1) && p.val != kValIdx;
-  const void* ksrc = keys_in;
-  const void* vsrc = p.val == kValIdx ? nullptr : vals_in;
+  SweepArgs a{};
+  a.keys[kBufIn] = keys_in;
+  a.keys[kBufAlt] = alt_keys;
+  a.keys[kBufOut] = keys_out;
+  a.vals[kBufIn] = p.val == kValU32 ? vals_in : nullptr;
+  a.vals[kBufAlt] = p.val == kValNone ? nullptr : alt_vals;
+  a.vals[kBufOut] = vals_out;
+  a.status_arr[0] = reinterpret_cast<uint32_t*>(at(temp, p.off_status0));
+  a.status_arr[1] = reinterpret_cast<uint32_t*>(at(temp, p.off_status1));
+  a.rows = p.rows;
+  a.cols = p.cols;
+  a.tiles_per_row = p.tiles_per_row;
+  a.full_per_row = p.cols / p.tile;
+  a.xf = xf;
+  a.bases_row_stride = static_cast<int64_t>(p.passes) * p.radix;
+  a.error = header + kHdrError;
+  a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  a.dynamic = dynamic ? 1 : 0;
+  uint32_t prev = kBufIn;
   for (int q = 0; q < p.passes; ++q) {
     const bool last = q == p.passes - 1;
-    bool to_out = odd_copy ? (q % 2 == 1) : ((p.passes - 1 - q) % 2 == 0);
-    SweepArgs a{};
-    a.keys_in = ksrc;
-    a.keys_out = to_out ? keys_out : alt_keys;
-    if (p.val == kValU32) {
-      a.vals_in = vsrc;
-      a.vals_out = to_out ? vals_out : alt_vals;
-    } else if (p.val == kValIdx) {
-      a.vals_in = vsrc;                       // null in the first pass: generate
-      a.vals_out = last ? vals_out : alt_vals;
-      a.wide_out = last ? 1 : 0;
+    a.code = pass_code(q, p.passes, prev, in_place);
+    prev = (a.code & kCodeDst) >> 2;
+    // the static schedule's buffers, as kernel arguments
+    const uint32_t src = a.code & kCodeSrc, dst = (a.code & kCodeDst) >> 2;
+    a.pass_keys_in = a.keys[src];
+    a.pass_keys_out = const_cast<void*>(a.keys[dst]);
+    if (p.val == kValIdx) {
+      a.pass_vals_in = q == 0 ? nullptr : alt_vals;
+      a.pass_vals_out = last ? vals_out : alt_vals;
+    } else {
+      a.pass_vals_in = a.vals[src];
+      a.pass_vals_out = const_cast<void*>(a.vals[dst]);
     }
-    a.rows = p.rows;
-    a.cols = p.cols;
-    a.tiles_per_row = p.tiles_per_row;
-    a.full_per_row = p.cols / p.tile;
+    a.pass_status = a.status_arr[q & 1];
+    a.pass_status_zero = last ? nullptr : a.status_arr[(q + 1) & 1];
     a.shift = p.begin_bit + q * p.bits;
     a.mask = last ? p.last_mask : static_cast<uint32_t>(p.radix - 1);
-    a.xf = xf;
     a.bases = bases + static_cast<size_t>(q) * p.radix;
-    a.bases_row_stride = static_cast<int64_t>(p.passes) * p.radix;
-    a.status = status[q & 1];
-    a.status_zero = last ? nullptr : status[(q + 1) & 1];
-    a.tile_counter = header + 1 + q;
-    a.error = header;
-    a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+    a.tile_counter = header + kHdrTileCounter + q;
     cudaError_t e = timed_launch(2, n, s, [&](int* k) { return sweep(p, a, k, s); });
     if (e != cudaSuccess) return RS_ERR_CUDA;
-    ksrc = a.keys_out;
-    vsrc = a.vals_out;
   }
-  if (odd_copy) {
-    if (cudaMemcpyAsync(keys_out, alt_keys, kb, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-      return RS_ERR_CUDA;
-    if (p.val == kValU32 &&
-        cudaMemcpyAsync(vals_out, alt_vals, vb_out, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
-      return RS_ERR_CUDA;
+  // no pass run, or an odd number run in place: copy (decided on the device)
+  FinishArgs f{};
+  f.passes_run = header + kHdrPassesRun;
+  f.in_place = in_place ? 1 : 0;
+  f.keys_in = keys_in;
+  f.keys_alt = alt_keys;
+  f.keys_out = keys_out;
+  f.keys_bytes = kb;
+  if (p.val == kValU32) {
+    f.vals_in = vals_in;
+    f.vals_alt = alt_vals;
+    f.vals_out = vals_out;
+    f.vals_bytes = vb_out;
+  }
+  if (p.val == kValIdx) f.idx_out = static_cast<int64_t*>(vals_out);
+  f.rows = p.rows;
+  f.cols = p.cols;
+  // (the static schedule needs it only in place with an odd number of passes)
+  if (dynamic || (in_place && p.passes % 2 == 1)) {
+    cudaError_t e = timed_launch(5, n, s, [&](int*) { return launch_finish(f, s); });
+    if (e != cudaSuccess) return RS_ERR_CUDA;
   }
   return RS_OK;
 }
@@ -422,7 +454,7 @@ rs_status radix_sort_histograms(const void* keys, int key_bytes, size_t n, int b
   if (n > 0 && !keys) return RS_ERR_INVALID;
   if (temp_bytes < p.total) return RS_ERR_TEMP_TOO_SMALL;
   if (reinterpret_cast<uintptr_t>(temp) % 256 != 0) return RS_ERR_INVALID;
-  return run_front(p, keys, KeyXform{0, 0}, temp, hist_out, bases_out,
+  return run_front(p, keys, KeyXform{0, 0}, temp, hist_out, bases_out, false, false,
                    static_cast<cudaStream_t>(stream));
 }
 
@@ -436,6 +468,18 @@ rs_status radix_sort_device_status(const void* temp, void* stream) {
   return word == kErrNone ? RS_OK : static_cast<rs_status>(word);
 }
 
+rs_status radix_sort_passes_run(const void* temp, int* passes, void* stream) {
+  if (!temp || !passes) return RS_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, static_cast<const uint32_t*>(temp) + kHdrPassesRun, 4,
+                      cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return RS_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RS_ERR_CUDA;
+  *passes = static_cast<int>(word);
+  return RS_OK;
+}
+
 const char* rs_status_string(rs_status status) {
   switch (status) {
     case RS_OK: return "RS_OK";
@@ -445,6 +489,12 @@ const char* rs_status_string(rs_status status) {
     case RS_ERR_LOOKBACK_TIMEOUT: return "RS_ERR_LOOKBACK_TIMEOUT";
   }
   return "RS_UNKNOWN";
+}
+
+rs_status rs_set_pass_skipping(int on) {
+  if (on != 0 && on != 1) return RS_ERR_INVALID;
+  g_pass_skipping.store(on, std::memory_order_relaxed);
+  return RS_OK;
 }
 
 rs_status rs_set_lookback_timeout_ns(uint64_t ns) {

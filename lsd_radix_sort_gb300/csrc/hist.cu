@@ -73,6 +73,51 @@ __global__ void __launch_bounds__(kScanThreads * Q) digit_scan_kernel(ScanArgs a
     a.bases[o] = excl;
     if (a.hist_out) a.hist_out[o] = total;
   }
+
+  // Without pass skipping every pass runs.
+  if (!a.dynamic) {
+    if (blockIdx.x == 0 && d == 0) a.header[kHdrPassesRun] = a.passes;
+    return;
+  }
+  // Pass p of this row is the identity when one digit holds every key of the
+  // row; record the passes where some row is not.  The last CTA to finish
+  // turns the flags into the schedule.
+  __shared__ int one_digit;
+  __shared__ bool last_cta;
+  if (d == 0) one_digit = 0;
+  asm volatile("bar.sync 1, %0;" ::"n"(kScanThreads));
+  if (d < a.radix && static_cast<int64_t>(total) == a.cols) one_digit = 1;
+  asm volatile("bar.sync 1, %0;" ::"n"(kScanThreads));
+  if (d == 0) {
+    uint32_t* hdr = a.header;
+    if (!one_digit) atomicOr(hdr + kHdrNontrivial + p, 1u);
+    __threadfence();
+    const uint32_t done = atomicAdd(hdr + kHdrScanDone, 1u);
+    last_cta = done == gridDim.x - 1;
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kScanThreads));
+  if (!last_cta) return;
+  __shared__ uint32_t nontrivial[kMaxPasses];
+  if (d < a.passes) {
+    __threadfence();
+    nontrivial[d] = ld_relaxed(a.header + kHdrNontrivial + d);
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kScanThreads));
+  if (d == 0) {
+    uint32_t m = 0;
+    for (int q = 0; q < a.passes; ++q) m += nontrivial[q] != 0;
+    uint32_t k = 0, prev = kBufIn;
+    for (int q = 0; q < a.passes; ++q) {
+      uint32_t code = kCodeSkip;
+      if (nontrivial[q] != 0) {
+        code = pass_code(k, m, prev, a.in_place != 0);
+        prev = (code & kCodeDst) >> 2;
+        ++k;
+      }
+      a.header[kHdrTileCounter + q] = code << kCodeShift;
+    }
+    a.header[kHdrPassesRun] = m;
+  }
 }
 
 }  // namespace

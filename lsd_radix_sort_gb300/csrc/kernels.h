@@ -103,21 +103,67 @@ struct HistArgs {
   size_t zero_words;
 };
 
+// Scratch header (u32 words): the device error word, one tile counter per
+// pass, and the pass schedule that K-SCAN derives from the histograms.
+constexpr int kHdrError = 0;
+constexpr int kHdrTileCounter = 1;     // + pass
+constexpr int kHdrScanDone = 65;       // K-SCAN CTAs finished
+constexpr int kHdrPassesRun = 66;      // passes the schedule executes
+constexpr int kHdrNontrivial = 128;    // + pass: some row has two digits in it
+constexpr int kMaxPasses = 64;
+
+// Buffers a pass reads or writes: the caller's input, the scratch
+// ping-pong buffer, the caller's output.
+enum PassBuf : uint32_t { kBufIn = 0, kBufAlt = 1, kBufOut = 2 };
+
+// The schedule.  A pass in which every row's keys share one digit is the
+// identity permutation (a stable scatter of one bucket) and is skipped; the
+// others alternate between the buffers so that the last one run writes the
+// caller's output (an in-place sort with an odd number of passes run ends
+// in the scratch buffer and is copied back).  K-SCAN writes each pass's
+// entry into the top byte of the pass's tile counter, so the atomic that
+// hands a CTA its tile also hands it the schedule: tile = value & kTileMask,
+// code = value >> kCodeShift.
+constexpr int kCodeShift = 24;
+constexpr uint32_t kTileMask = (1u << kCodeShift) - 1;
+constexpr uint32_t kCodeSrc = 0x03;    // PassBuf of the keys (and u32 payloads) read
+constexpr uint32_t kCodeDst = 0x0C;    // PassBuf written, << 2
+constexpr uint32_t kCodeOdd = 0x10;    // odd index among the passes run: look-back array 1
+constexpr uint32_t kCodeFirst = 0x20;  // first pass run
+constexpr uint32_t kCodeLast = 0x40;   // last pass run
+constexpr uint32_t kCodeSkip = 0x80;   // identity pass: not run
+
 struct ScanArgs {
   const uint32_t* slots;
   int64_t rows;
+  int64_t cols;
   int chunks_per_row;
   int passes;
   int radix;
   uint32_t* hist_out;      // optional [rows][passes][radix] totals
   uint32_t* bases;         // [rows][passes][radix] exclusive scans
+  uint32_t* header;        // scratch header: nontrivial flags, schedule
+  int in_place;            // the sort reads and writes the same buffer
+  int dynamic;             // write the schedule codes into the tile counters
 };
 
+// The schedule code of pass k of m run (host and K-SCAN use the same rule):
+// pass 0 reads the input; in place, the passes alternate starting with the
+// scratch buffer, otherwise they end on the output.
+inline __host__ __device__ uint32_t pass_code(uint32_t k, uint32_t m, uint32_t src,
+                                              bool in_place) {
+  const bool to_out = in_place ? (k % 2 == 1) : ((m - 1 - k) % 2 == 0);
+  const uint32_t dst = to_out ? kBufOut : kBufAlt;
+  return src | (dst << 2) | ((k & 1) ? kCodeOdd : 0u) | (k == 0 ? kCodeFirst : 0u) |
+         (k + 1 == m ? kCodeLast : 0u);
+}
+
 struct SweepArgs {
-  const void* keys_in;
-  void* keys_out;
-  const void* vals_in;     // null with kValIdx: generate column indices
-  void* vals_out;
+  // buffers by PassBuf: the caller's input, the scratch buffer, the output
+  // (kValIdx: vals[kBufIn] is unused, indices are generated by the first
+  // pass run; vals[kBufAlt] holds int32 indices, vals[kBufOut] int64)
+  const void* keys[3];
+  const void* vals[3];
   int64_t rows, cols;
   int64_t tiles_per_row;
   int64_t full_per_row;    // tiles of a row that hold a whole tile of keys
@@ -125,12 +171,18 @@ struct SweepArgs {
   int shift;
   uint32_t mask;
   KeyXform xf;             // key transform
-  int wide_out;            // kValIdx: write int64 indices
   const uint32_t* bases;   // bases of this pass for row 0
   int64_t bases_row_stride;
-  uint32_t* status;        // [rows * tiles_per_row][radix] look-back words
-  uint32_t* status_zero;   // next pass's look-back words, zeroed here
-  uint32_t* tile_counter;
+  uint32_t* status_arr[2]; // look-back words [rows * full_per_row][radix], by parity
+  uint32_t* tile_counter;  // (schedule code << kCodeShift, when dynamic) | tiles handed out
+  int dynamic;             // the schedule comes from K-SCAN (pass skipping on)
+  uint32_t code;           // otherwise: this pass's code, from the host, and
+  const void* pass_keys_in;   // the buffers and look-back words it selects
+  void* pass_keys_out;
+  const void* pass_vals_in;
+  void* pass_vals_out;
+  uint32_t* pass_status;
+  uint32_t* pass_status_zero;
   uint32_t* error;
   uint64_t timeout_ns;
 };
@@ -150,6 +202,25 @@ cudaError_t launch_sweep_x64(ValKind v, int bits, const SweepArgs& a, int* launc
                              cudaStream_t s);
 cudaError_t launch_sweep_f16(const SweepArgs& a, int* launched, cudaStream_t s);
 cudaError_t launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t s);
+// After the passes: when no pass ran (every pass was the identity) copy the
+// input to the output, and write column indices as the identity; when an
+// in-place sort ran an odd number of passes, copy the scratch buffers back.
+// Decided on the device from the schedule; otherwise nothing is done.
+struct FinishArgs {
+  const uint32_t* passes_run;
+  int in_place;
+  const void* keys_in;
+  const void* keys_alt;
+  void* keys_out;
+  size_t keys_bytes;       // multiple of 2
+  const void* vals_in;     // u32 payloads (or null)
+  const void* vals_alt;
+  void* vals_out;
+  size_t vals_bytes;       // multiple of 2; 0 without u32 payloads
+  int64_t* idx_out;        // column indices (row-wise sort) or null
+  int64_t rows, cols;
+};
+cudaError_t launch_finish(const FinishArgs& f, cudaStream_t s);
 cudaError_t launch_timeout_probe(uint32_t* word, uint32_t* error, uint64_t timeout_ns,
                                  cudaStream_t s);
 

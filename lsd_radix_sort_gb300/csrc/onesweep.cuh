@@ -197,6 +197,52 @@ struct TileScratch {
   alignas(16) uint32_t warp_cnt[W][R];  // per-warp digit counters, then per-warp offsets
   uint32_t warp_tot[W];     // per-warp sums of the digit-count scan
   uint32_t g_off[R];        // output position of staged slot j is g_off[d] + j
+  uint32_t code;            // this pass's schedule code (kCode* bits)
+};
+
+// This pass's buffers and look-back arrays, picked from the kernel
+// parameters by the schedule entry (so that the compiler still sees global
+// pointers).
+template <class P>
+__device__ __forceinline__ P pick_buf(const P (&b)[3], uint32_t i) {
+  return i == kBufIn ? b[0] : (i == kBufAlt ? b[1] : b[2]);
+}
+
+template <bool DYN>
+struct PassBufs {
+  uint32_t code;
+  const SweepArgs& a;
+  __device__ __forceinline__ bool first() const { return code & kCodeFirst; }
+  __device__ __forceinline__ bool last() const { return code & kCodeLast; }
+  __device__ __forceinline__ uint32_t src() const { return code & kCodeSrc; }
+  __device__ __forceinline__ uint32_t dst() const { return (code & kCodeDst) >> 2; }
+  __device__ __forceinline__ const void* keys_in() const {
+    return DYN ? pick_buf(a.keys, src()) : a.pass_keys_in;
+  }
+  __device__ __forceinline__ void* keys_out() const {
+    return DYN ? const_cast<void*>(pick_buf(a.keys, dst())) : a.pass_keys_out;
+  }
+  // column indices (kValIdx): int32 in the scratch buffer, int64 at the end;
+  // the first pass run generates them
+  template <int VK>
+  __device__ __forceinline__ const void* vals_in() const {
+    if (!DYN) return a.pass_vals_in;
+    if (VK == kValIdx) return first() ? nullptr : a.vals[kBufAlt];
+    return pick_buf(a.vals, src());
+  }
+  template <int VK>
+  __device__ __forceinline__ void* vals_out() const {
+    if (!DYN) return a.pass_vals_out;
+    if (VK == kValIdx) return const_cast<void*>(last() ? a.vals[kBufOut] : a.vals[kBufAlt]);
+    return const_cast<void*>(pick_buf(a.vals, dst()));
+  }
+  __device__ __forceinline__ uint32_t* status() const {
+    return DYN ? a.status_arr[(code & kCodeOdd) ? 1 : 0] : a.pass_status;
+  }
+  __device__ __forceinline__ uint32_t* status_zero() const {
+    if (!DYN) return a.pass_status_zero;
+    return last() ? nullptr : a.status_arr[(code & kCodeOdd) ? 0 : 1];
+  }
 };
 
 // Where a tile's keys and payloads are read from and staged to.  The key
@@ -213,7 +259,7 @@ struct TileIo {
 
 // One tile: rank, publish, look back, stage, write.  Called by every thread
 // of the CTA; begins and ends with all threads converged.
-template <bool FULL, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
+template <bool FULL, bool DYN, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
 __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
                                            TileScratch<THREADS / kWarp, (1 << BITS)>& s,
                                            const TileIo<KeyOp>& io, uint32_t* status_row,
@@ -374,10 +420,11 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   LSDRS_PHASE(5);  // wait for the slowest digit's look-back
 
   // ---- 7. contiguous per-digit runs out ---------------------------------
-  T* kout = static_cast<T*>(a.keys_out) + row_base;
-  uint32_t* vout32 = static_cast<uint32_t*>(a.vals_out) + row_base;
-  int64_t* vout64 = static_cast<int64_t*>(a.vals_out) + row_base;
-  const bool wide = VK == kValIdx && a.wide_out;
+  const PassBufs<DYN> pb{DYN ? s.code : a.code, a};
+  T* kout = static_cast<T*>(pb.keys_out()) + row_base;
+  uint32_t* vout32 = static_cast<uint32_t*>(pb.template vals_out<VK>()) + row_base;
+  int64_t* vout64 = static_cast<int64_t*>(pb.template vals_out<VK>()) + row_base;
+  const bool wide = VK == kValIdx && pb.last();
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
     const int j = i * THREADS + tid;
@@ -418,7 +465,10 @@ struct SweepSmem {
 // tile of each row (CTA r takes row r's).  Within a row no tile waits on the
 // partial one, so the tail kernel runs after the full tiles are done; keeping
 // it out of the full-tile kernel leaves that kernel's registers to full tiles.
-template <bool TAIL, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
+// DYN: the schedule (which passes run, between which buffers) comes from
+// K-SCAN through the tile counter; otherwise it is the host's static one in
+// the kernel arguments (every pass runs).
+template <bool TAIL, bool DYN, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
 __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
   using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
   using T = typename KeyOp::T;
@@ -432,8 +482,11 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
   S& s = *reinterpret_cast<S*>(smem_raw);
   const int tid = threadIdx.x;
 
+  // the tile id and this pass's schedule code in one word
   if (tid == 0) {
-    s.tile_id = TAIL ? 0u : atomicAdd(a.tile_counter, 1u);
+    const uint32_t v = TAIL ? ld_relaxed(a.tile_counter) : atomicAdd(a.tile_counter, 1u);
+    s.tile_id = v & kTileMask;
+    if (DYN) s.scratch.code = v >> kCodeShift;
     s.abort = ld_relaxed(a.error) != kErrNone;
   }
   static_assert((W * R) % 4 == 0, "counters are zeroed 16 bytes at a time");
@@ -455,13 +508,15 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
     t = id - r32 * fpr;
     tile_begin = t * TILE;
   }
-  // look-back words are indexed by full tile, row-major: row r's tile t at
-  // r * full_per_row + t; partial tiles publish none
-  uint32_t* status_row = a.status + (row * a.full_per_row) * R;
   const int valid = TAIL ? static_cast<int>(a.cols - tile_begin) : TILE;
   const int64_t off = row * a.cols + tile_begin;
+  if (DYN && (s.scratch.code & kCodeSkip)) return;  // an identity pass: not run
+  const PassBufs<DYN> pb{DYN ? s.scratch.code : a.code, a};
+  // look-back words are indexed by full tile, row-major: row r's tile t at
+  // r * full_per_row + t; partial tiles publish none
+  uint32_t* status_row = pb.status() + (row * a.full_per_row) * R;
   TileIo<KeyOp> io;
-  io.key_src = static_cast<const T*>(a.keys_in) + off;
+  io.key_src = static_cast<const T*>(pb.keys_in()) + off;
   io.stage_keys = s.stage;
   io.vals = s.vals;
   io.val_bar = nullptr;
@@ -469,13 +524,13 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
   if (s.abort) {  // an earlier tile failed: release successors and stop
     if (!TAIL && tid < R) st_relaxed(status_row + t * R + tid, kFlagP);
   } else {
-    if (VK != kValNone && a.vals_in != nullptr) {
+    if (VK != kValNone && pb.template vals_in<VK>() != nullptr) {
       // Payloads are not needed before the staging step: a full tile with an
       // aligned source gets them by one bulk copy issued now (the tile's
       // first block-wide barrier orders the barrier's initialisation before
       // any thread waits on it); otherwise the CTA copies them, and the same
       // barrier makes them visible.
-      const uint32_t* vsrc = static_cast<const uint32_t*>(a.vals_in) + off;
+      const uint32_t* vsrc = static_cast<const uint32_t*>(pb.template vals_in<VK>()) + off;
       io.vals_in = true;
       if (LSDRS_VALS_TMA && !TAIL && (reinterpret_cast<uintptr_t>(vsrc) & 15) == 0) {
         if (tid == 0) {
@@ -488,21 +543,21 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
         for (int i = tid; i < valid; i += THREADS) s.vals[i] = ld_stream(vsrc + i);
       }
     }
-    sweep_tile<!TAIL, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io, status_row, row, t,
+    sweep_tile<!TAIL, DYN, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io, status_row, row, t,
                                                            tile_begin, valid);
   }
-  if (!TAIL && a.status_zero != nullptr && tid < R)
-    a.status_zero[static_cast<int64_t>(s.tile_id) * R + tid] = 0;
+  uint32_t* zero = PassBufs<DYN>{DYN ? s.scratch.code : a.code, a}.status_zero();
+  if (!TAIL && zero != nullptr && tid < R) zero[static_cast<int64_t>(s.tile_id) * R + tid] = 0;
 }
 
-template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB, int WIN>
+template <bool DYN, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB, int WIN>
 __global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
-  onesweep_body<false, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a);
+  onesweep_body<false, DYN, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a);
 }
 
-template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
+template <bool DYN, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
 __global__ void __launch_bounds__(THREADS, 1) onesweep_tail_kernel(SweepArgs a) {
-  onesweep_body<true, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a);
+  onesweep_body<true, DYN, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a);
 }
 
 template <class K>
@@ -536,15 +591,24 @@ cudaError_t launch_sweep_t(const SweepArgs& args, int* launched, cudaStream_t s)
   *launched = 0;
   const int64_t full = a.rows * a.full_per_row;
   if (full > 0) {
-    cudaError_t e = launch_with_smem(onesweep_kernel<KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>,
-                                     static_cast<unsigned>(full), THREADS, sizeof(S), s, a);
+    cudaError_t e =
+        a.dynamic
+            ? launch_with_smem(onesweep_kernel<true, KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>,
+                               static_cast<unsigned>(full), THREADS, sizeof(S), s, a)
+            : launch_with_smem(onesweep_kernel<false, KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>,
+                               static_cast<unsigned>(full), THREADS, sizeof(S), s, a);
     if (e != cudaSuccess) return e;
     ++*launched;
   }
   if (a.rows > 0 && a.cols % TILE != 0) {
-    cudaError_t e = launch_with_smem(
-        onesweep_tail_kernel<KeyOp, BITS, VK, kTailThreads, TAIL_ITEMS, WIN>,
-        static_cast<unsigned>(a.rows), kTailThreads, sizeof(ST), s, a);
+    cudaError_t e =
+        a.dynamic
+            ? launch_with_smem(onesweep_tail_kernel<true, KeyOp, BITS, VK, kTailThreads,
+                                                    TAIL_ITEMS, WIN>,
+                               static_cast<unsigned>(a.rows), kTailThreads, sizeof(ST), s, a)
+            : launch_with_smem(onesweep_tail_kernel<false, KeyOp, BITS, VK, kTailThreads,
+                                                    TAIL_ITEMS, WIN>,
+                               static_cast<unsigned>(a.rows), kTailThreads, sizeof(ST), s, a);
     if (e != cudaSuccess) return e;
     ++*launched;
   }

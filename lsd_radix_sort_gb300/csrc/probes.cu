@@ -63,6 +63,62 @@ cudaError_t launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t s
   return cudaGetLastError();
 }
 
+// The finishing step of a sort (see FinishArgs), grid-stride, in the widest
+// units that the pointers' alignment and the size allow (16, 4 or 2 bytes:
+// every key and payload size is a multiple of 2).
+template <class U>
+__device__ __forceinline__ void copy_units(void* dst, const void* src, size_t units) {
+  U* d = static_cast<U*>(dst);
+  const U* s = static_cast<const U*>(src);
+  const size_t stride = static_cast<size_t>(gridDim.x) * kCopyThreads;
+  for (size_t i = static_cast<size_t>(blockIdx.x) * kCopyThreads + threadIdx.x; i < units;
+       i += stride)
+    __stcs(d + i, __ldcs(s + i));
+}
+
+__device__ __forceinline__ void copy_bytes(void* dst, const void* src, size_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) | bytes;
+  if ((a & 15) == 0)
+    copy_units<uint4>(dst, src, bytes / 16);
+  else if ((a & 3) == 0)
+    copy_units<uint32_t>(dst, src, bytes / 4);
+  else
+    copy_units<unsigned short>(dst, src, bytes / 2);
+}
+
+__global__ void __launch_bounds__(kCopyThreads) finish_kernel(FinishArgs f) {
+  const uint32_t m = *f.passes_run;
+  const void* ksrc = nullptr;
+  const void* vsrc = nullptr;
+  if (m == 0) {
+    ksrc = f.keys_in;
+    vsrc = f.vals_in;
+    if (f.idx_out != nullptr) {
+      const size_t n = static_cast<size_t>(f.rows) * static_cast<size_t>(f.cols);
+      const size_t stride = static_cast<size_t>(gridDim.x) * kCopyThreads;
+      for (size_t i = static_cast<size_t>(blockIdx.x) * kCopyThreads + threadIdx.x; i < n;
+           i += stride)
+        f.idx_out[i] = static_cast<int64_t>(i % static_cast<size_t>(f.cols));
+    }
+  } else if (f.in_place && (m & 1u)) {
+    ksrc = f.keys_alt;
+    vsrc = f.vals_alt;
+  }
+  if (ksrc != nullptr && ksrc != f.keys_out) copy_bytes(f.keys_out, ksrc, f.keys_bytes);
+  if (vsrc != nullptr && vsrc != f.vals_out && f.vals_bytes)
+    copy_bytes(f.vals_out, vsrc, f.vals_bytes);
+}
+
+cudaError_t launch_finish(const FinishArgs& f, cudaStream_t s) {
+  if (f.keys_bytes % 2 || f.vals_bytes % 2) return cudaErrorInvalidValue;
+  const size_t units = (f.keys_bytes > f.vals_bytes ? f.keys_bytes : f.vals_bytes) / 16;
+  size_t grid = (units + kCopyThreads - 1) / kCopyThreads;
+  if (grid > 4 * 152) grid = 4 * 152;
+  if (grid == 0) grid = 1;
+  finish_kernel<<<static_cast<unsigned>(grid), kCopyThreads, 0, s>>>(f);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_timeout_probe(uint32_t* word, uint32_t* error, uint64_t timeout_ns,
                                  cudaStream_t s) {
   timeout_probe_kernel<<<1, 1, 0, s>>>(word, error, timeout_ns);
