@@ -3,6 +3,7 @@ payload, 8-bit digits (4 passes), on one GB300 (or N independent replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--n LOG2] [--no-distributions] [--no-e2e] [--no-cpu-baseline]
+                    [--no-copy-probe] [--no-small-sorts]
 
 Prints one JSON line on rank 0.  `value` is sorted keys per second with the
 inputs already in HBM (inputs of 2 GiB, larger than L2, so no flush is
@@ -10,8 +11,12 @@ needed); `e2e` is the same sort through the C ABI with the keys and payloads
 copied from pinned host memory and the result copied back inside the timed
 region.  `roofline` reports the onesweep scatter kernel (the dominant one)
 against the measured HBM copy bandwidth; `cpu_baseline` times the CPU oracle
-on a bounded sample of the same workload.  Under torchrun each rank sorts its
-own replica (the sort has no exchange step); the time is the max over ranks.
+on a bounded sample of the same workload.  `distributions` times the other
+key distributions of the same workload, each also with pass skipping on
+(reported apart from the ideal-bytes model, since identity passes are not
+run); `small_sorts` compares stream launches with CUDA-graph replay of the
+same sort from 2^10 to 2^20 keys.  Under torchrun each rank sorts its own
+replica (the sort has no exchange step); the time is the max over ranks.
 """
 from __future__ import annotations
 
@@ -167,6 +172,53 @@ def barrier(world: int):
         dist.barrier()
 
 
+def small_sort_latency(rs, torch, workloads, log2_sizes, reps: int = 200):
+    """Per-sort time of small key-value sorts launched on a stream and replayed
+    from a CUDA graph that captured the same call (the launch sequence of a
+    sort is fixed and needs no host synchronisation, so one call captures)."""
+    import numpy as np
+    out = {}
+    stream = torch.cuda.current_stream()
+    for lg in log2_sizes:
+        n = 1 << lg
+        dk = torch.from_numpy(workloads.u32_uniform(n, lg).view(np.int32)).cuda()
+        dv = torch.from_numpy(workloads.index_payload(n).view(np.int32)).cuda()
+        ko, vo = torch.empty_like(dk), torch.empty_like(dv)
+        temp = torch.empty(rs.temp_bytes(n, 4, 4, 0, 32, DIGIT_BITS), dtype=torch.uint8,
+                           device="cuda")
+
+        def sort():
+            rs.radix_sort_pairs(dk, dv, ko, vo, 0, 32, DIGIT_BITS, temp=temp)
+
+        def timed(fn):
+            for _ in range(10):
+                fn()
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) * 1e3 / reps
+        t_stream = timed(sort)
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                sort()
+        stream.wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            sort()
+        t_graph = timed(g.replay)
+        out[f"2^{lg}"] = {"stream_us": round(t_stream, 2), "graph_us": round(t_graph, 2),
+                          "graph_saves": round(1 - t_graph / t_stream, 3)}
+        del g, dk, dv, ko, vo, temp
+    return out
+
+
 def cpu_oracle_rate(n_sample: int, reps: int = 1):
     """Time the CPU oracle (as it stands, one thread) on a sample of the workload."""
     import oracle
@@ -240,6 +292,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-copy-probe", action="store_true")
+    ap.add_argument("--no-small-sorts", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -391,6 +444,19 @@ def main():
                                  stream)
             dists[name] = {"ms": dms, "gkeys_s": n / (dms * 1e-3) / 1e9,
                            "hbm_frac": total_ideal / (dms * 1e-3) / 1e9 / peak}
+            if name != "uniform":
+                # the same sort with pass skipping on: identity passes are not
+                # run, so the ideal-bytes model above does not apply
+                rs.set_pass_skipping(True)
+                sms = time_sorts(rs, torch, dk, dv, ko, vo, temp, max(args.steps // 2, 3), 3,
+                                 stream)
+                dists[name]["pass_skipping"] = {"ms": sms, "gkeys_s": n / (sms * 1e-3) / 1e9,
+                                                "passes_run": rs.passes_run(temp)}
+                rs.set_pass_skipping(False)
+
+    small = None
+    if not args.no_small_sorts:
+        small = small_sort_latency(rs, torch, workloads, (10, 12, 14, 16, 18, 20))
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -414,7 +480,7 @@ def main():
                         "frac_of_peak": total_ideal / (ms_max * 1e-3) / 1e9 / peak},
                 "e2e": e2e, "gpu_launches": launches, "kernels": kernels,
                 "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks,
-                "distributions": dists}
+                "distributions": dists, "small_sorts": small}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
