@@ -3,7 +3,7 @@ payload, 8-bit digits (4 passes), on one GB300 (or N independent replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--n LOG2] [--no-distributions] [--no-e2e] [--no-cpu-baseline]
-                    [--no-copy-probe] [--no-small-sorts]
+                    [--no-copy-probe] [--no-small-sorts] [--no-rows]
 
 Prints one JSON line on rank 0.  `value` is sorted keys per second with the
 inputs already in HBM (inputs of 2 GiB, larger than L2, so no flush is
@@ -15,7 +15,9 @@ on a bounded sample of the same workload.  `distributions` times the other
 key distributions of the same workload, each also with pass skipping on
 (reported apart from the ideal-bytes model, since identity passes are not
 run); `small_sorts` compares stream launches with CUDA-graph replay of the
-same sort from 2^10 to 2^20 keys.  Under torchrun each rank sorts its own
+same sort from 2^10 to 2^20 keys; `row_sorts` times the row-wise fp16 sort
+on the FlagTree H20 shapes with both ways of finding tile offsets, beside
+torch.sort.  Under torchrun each rank sorts its own
 replica (the sort has no exchange step); the time is the max over ranks.
 """
 from __future__ import annotations
@@ -219,6 +221,45 @@ def small_sort_latency(rs, torch, workloads, log2_sizes, reps: int = 200):
     return out
 
 
+ROW_SHAPES = [(64, 64), (256, 256), (1024, 1024), (4096, 4096), (1024, 65536), (1024, 1),
+              (1024, 512), (16, 131072), (8, 262144)]
+
+
+def row_sorts(rs, torch, workloads, reps: int = 20):
+    """Row-wise fp16 sorts on the FlagTree PR #1084 H20 shapes (ascending,
+    last dimension): torch.sort, and this library with the tile offsets found
+    by the look-back and precomputed before each pass."""
+    import numpy as np
+    out = {}
+    for rows, cols in ROW_SHAPES:
+        x = torch.from_numpy(workloads.rows16(rows, cols, "f16", 0).view(np.int16)).cuda()
+        x = x.view(torch.float16)
+        v = torch.empty_like(x)
+        idx = torch.empty((rows, cols), dtype=torch.int64, device="cuda")
+        temp = torch.empty(rs.segmented_temp_bytes(rows, cols), dtype=torch.uint8, device="cuda")
+
+        def timed(fn):
+            for _ in range(5):
+                fn()
+            torch.cuda.synchronize()
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            for _ in range(reps):
+                fn()
+            b.record()
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / reps
+        entry = {"torch_sort_ms": round(timed(lambda: torch.sort(x, dim=-1)), 4)}
+        for mode, name in ((False, "lookback_ms"), (True, "precomputed_ms")):
+            rs.set_tile_offsets(mode)
+            entry[name] = round(timed(lambda: rs.segmented_sort(x, False, v, idx, temp)), 4)
+        rs.set_tile_offsets(False)
+        out[f"{rows}x{cols}"] = entry
+        del x, v, idx, temp
+    return out
+
+
 def cpu_oracle_rate(n_sample: int, reps: int = 1):
     """Time the CPU oracle (as it stands, one thread) on a sample of the workload."""
     import oracle
@@ -293,6 +334,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-copy-probe", action="store_true")
     ap.add_argument("--no-small-sorts", action="store_true")
+    ap.add_argument("--no-rows", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -457,6 +499,9 @@ def main():
     small = None
     if not args.no_small_sorts:
         small = small_sort_latency(rs, torch, workloads, (10, 12, 14, 16, 18, 20))
+    rows_tab = None
+    if not args.no_rows:
+        rows_tab = row_sorts(rs, torch, workloads)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -480,7 +525,7 @@ def main():
                         "frac_of_peak": total_ideal / (ms_max * 1e-3) / 1e9 / peak},
                 "e2e": e2e, "gpu_launches": launches, "kernels": kernels,
                 "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks,
-                "distributions": dists, "small_sorts": small}
+                "distributions": dists, "small_sorts": small, "row_sorts": rows_tab}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -196,6 +196,17 @@ rs_status radix_sort_device_status(const void* temp, void* stream);
  *   on   0 or 1 (anything else: RS_ERR_INVALID) */
 rs_status rs_set_pass_skipping(int on);
 
+/* How the row-wise sort finds each tile's output offsets, for every
+ * row-wise sort enqueued after the call (process-wide):
+ *   0 (default) decoupled look-back inside the scatter pass;
+ *   1           precomputed: before each pass, a kernel counts the digits of
+ *               every tile and a per-row scan turns the counts into offsets,
+ *               so the scatter never waits on another tile (FlagTree PR
+ *               #1084, section 2, "precompute each tile"); it reads the keys
+ *               once more per pass.  Pass skipping does not apply in this mode.
+ * Anything else: RS_ERR_INVALID.  The results are identical. */
+rs_status rs_set_tile_offsets(int precomputed);
+
 /* Passes run by the last sort enqueued with this scratch buffer (all of
  * them unless pass skipping is on).  Synchronises `stream` and reads the
  * count.

@@ -23,7 +23,7 @@ from . import build as _build
 __all__ = [
     "RadixSortError", "load_library", "library_path", "temp_bytes", "radix_sort_keys",
     "radix_sort_pairs", "segmented_sort", "segmented_temp_bytes", "upfront_histograms",
-    "device_status", "passes_run", "set_pass_skipping", "copy_probe", "set_lookback_timeout_ns", "lookback_timeout_probe",
+    "device_status", "passes_run", "set_pass_skipping", "set_tile_offsets", "copy_probe", "set_lookback_timeout_ns", "lookback_timeout_probe",
     "profile_enable", "profile_read", "launch_count_reset", "EXPORTED_SYMBOLS",
 ]
 
@@ -33,7 +33,8 @@ KEY_TYPES = {"u32": (0, 4), "i32": (1, 4), "f32": (2, 4), "u64": (3, 8), "i64": 
              "f64": (5, 8)}
 RS_MAX_KEYS = (1 << 30) - 1
 KERNEL_NAMES = {0: "upfront_hist", 1: "digit_scan", 2: "onesweep", 3: "copy_probe",
-                4: "timeout_probe", 5: "finish"}
+                4: "timeout_probe", 5: "finish", 6: "tile_counts",
+                7: "small_sort"}
 
 EXPORTED_SYMBOLS = (
     "radix_sort_temp_bytes", "radix_sort_keys_u32", "radix_sort_keys_u64",
@@ -42,7 +43,7 @@ EXPORTED_SYMBOLS = (
     "rs_status_string", "rs_set_lookback_timeout_ns", "rs_lookback_timeout_probe",
     "rs_copy_probe", "rs_profile_enable", "rs_profile_read", "rs_launch_count_reset",
     "radix_sort_pairs_u32_noalloc", "radix_sort_keys_typed", "radix_sort_pairs_typed",
-    "radix_sort_passes_run", "rs_set_pass_skipping",
+    "radix_sort_passes_run", "rs_set_pass_skipping", "rs_set_tile_offsets",
 )
 
 
@@ -102,6 +103,7 @@ def load_library() -> ctypes.CDLL:
             "radix_sort_keys_typed": [i, i, P, P, sz, i, i, i, P, sz, P],
             "radix_sort_passes_run": [P, P, P],
             "rs_set_pass_skipping": [i],
+            "rs_set_tile_offsets": [i],
             "radix_sort_pairs_typed": [i, i, P, P, P, P, sz, i, i, i, P, sz, P],
         }
         for name, args in sig.items():
@@ -309,6 +311,12 @@ def upfront_histograms(keys, begin_bit: int = 0, end_bit: int | None = None,
                                      t.numel() * t.element_size(), _stream_ptr(stream)),
            "radix_sort_histograms")
     return hist[:passes], bases[:passes]
+
+
+def set_tile_offsets(precomputed: bool):
+    """Row-wise sorts: precompute each tile's output offsets before every pass
+    (True) instead of the decoupled look-back (False, the default)."""
+    _check(load_library().rs_set_tile_offsets(int(bool(precomputed))), "rs_set_tile_offsets")
 
 
 def set_pass_skipping(on: bool):

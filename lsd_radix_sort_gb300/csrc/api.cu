@@ -16,6 +16,7 @@ namespace {
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_pass_skipping{0};
+std::atomic<int> g_tile_offsets{0};
 
 // ---------------------------------------------------------------- profiling
 struct ProfRec {
@@ -76,7 +77,8 @@ struct Plan {
   int64_t tiles_per_row, tiles;
   int chunks_per_row;
   int64_t chunk_len;
-  size_t off_status0, off_status1, off_bases, off_slots, off_alt_keys, off_alt_vals, total;
+  size_t off_status0, off_status1, off_bases, off_slots, off_tile_offsets, off_alt_keys,
+      off_alt_vals, total;
 };
 
 rs_status make_plan(KeyKind key, ValKind val, int64_t rows, int64_t cols, int begin_bit,
@@ -124,6 +126,8 @@ rs_status make_plan(KeyKind key, ValKind val, int64_t rows, int64_t cols, int be
   off += align_up(static_cast<size_t>(rows) * p.passes * p.radix * 4, 256);
   p.off_slots = off;
   off += align_up(static_cast<size_t>(rows) * p.chunks_per_row * p.passes * p.radix * 4, 256);
+  p.off_tile_offsets = off;  // row-wise sorts: precomputed tile offsets of one pass
+  if (val == kValIdx) off += align_up(static_cast<size_t>(p.tiles) * p.radix * 4, 256);
   p.off_alt_keys = off;
   off += align_up(n * p.key_bytes, 256);
   p.off_alt_vals = off;
@@ -232,7 +236,30 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
 
   if (p.val == kValIdx && p.passes > 2) return RS_ERR_INVALID;  // 16-bit keys: two passes
 
-  const bool dynamic = g_pass_skipping.load(std::memory_order_relaxed) != 0;
+  // rows of at most one small tile: the whole sort in one kernel
+  if (small_sort_fits(p.key, p.val, p.bits, p.cols)) {
+    SmallArgs sa{};
+    sa.keys_in = keys_in;
+    sa.keys_out = keys_out;
+    sa.vals_in = vals_in;
+    sa.vals_out = vals_out;
+    sa.rows = p.rows;
+    sa.cols = p.cols;
+    sa.begin_bit = p.begin_bit;
+    sa.passes = p.passes;
+    sa.last_mask = p.last_mask;
+    sa.xf = xf;
+    sa.header = reinterpret_cast<uint32_t*>(temp);
+    cudaError_t e = timed_launch(7, n, s, [&](int*) {
+      return launch_small(p.key, p.val, p.bits, sa, s);
+    });
+    return e == cudaSuccess ? RS_OK : RS_ERR_CUDA;
+  }
+
+  // row-wise sorts may take precomputed tile offsets instead of the
+  // look-back; that mode keeps the static schedule (every pass runs)
+  const bool precomputed = p.val == kValIdx && g_tile_offsets.load(std::memory_order_relaxed) != 0;
+  const bool dynamic = !precomputed && g_pass_skipping.load(std::memory_order_relaxed) != 0;
   rs_status st = run_front(p, keys_in, xf, temp, nullptr, nullptr, in_place, dynamic, s);
   if (st != RS_OK) return st;
 
@@ -283,6 +310,26 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
     a.mask = last ? p.last_mask : static_cast<uint32_t>(p.radix - 1);
     a.bases = bases + static_cast<size_t>(q) * p.radix;
     a.tile_counter = header + kHdrTileCounter + q;
+    if (precomputed) {
+      TileCountArgs tc{};
+      tc.keys = a.pass_keys_in;
+      tc.rows = p.rows;
+      tc.cols = p.cols;
+      tc.tiles_per_row = p.tiles_per_row;
+      tc.tile = p.tile;
+      tc.shift = a.shift;
+      tc.mask = a.mask;
+      tc.xf = xf;
+      tc.bases = a.bases;
+      tc.bases_row_stride = a.bases_row_stride;
+      tc.offsets = reinterpret_cast<uint32_t*>(at(temp, p.off_tile_offsets));
+      a.offsets = tc.offsets;
+      cudaError_t e = timed_launch(6, n, s, [&](int* k) {
+        *k = 2;
+        return launch_tile_counts_f16(tc, s);
+      });
+      if (e != cudaSuccess) return RS_ERR_CUDA;
+    }
     cudaError_t e = timed_launch(2, n, s, [&](int* k) { return sweep(p, a, k, s); });
     if (e != cudaSuccess) return RS_ERR_CUDA;
   }
@@ -494,6 +541,12 @@ const char* rs_status_string(rs_status status) {
 rs_status rs_set_pass_skipping(int on) {
   if (on != 0 && on != 1) return RS_ERR_INVALID;
   g_pass_skipping.store(on, std::memory_order_relaxed);
+  return RS_OK;
+}
+
+rs_status rs_set_tile_offsets(int precomputed) {
+  if (precomputed != 0 && precomputed != 1) return RS_ERR_INVALID;
+  g_tile_offsets.store(precomputed, std::memory_order_relaxed);
   return RS_OK;
 }
 

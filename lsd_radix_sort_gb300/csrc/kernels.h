@@ -183,6 +183,7 @@ struct SweepArgs {
   void* pass_vals_out;
   uint32_t* pass_status;
   uint32_t* pass_status_zero;
+  const uint32_t* offsets; // [rows * tiles_per_row][radix] precomputed output offsets, or null
   uint32_t* error;
   uint64_t timeout_ns;
 };
@@ -201,6 +202,39 @@ cudaError_t launch_sweep_x32(ValKind v, int bits, const SweepArgs& a, int* launc
 cudaError_t launch_sweep_x64(ValKind v, int bits, const SweepArgs& a, int* launched,
                              cudaStream_t s);
 cudaError_t launch_sweep_f16(const SweepArgs& a, int* launched, cudaStream_t s);
+
+// Precomputed tile offsets (row-wise sorts, instead of the look-back): per
+// pass, the digit counts of every tile of the pass's input, then per row and
+// digit an exclusive scan over the row's tiles plus the digit's base.
+struct TileCountArgs {
+  const void* keys;        // the pass's input keys
+  int64_t rows, cols, tiles_per_row;
+  int tile;                // keys per tile (the sweep's)
+  int shift;
+  uint32_t mask;
+  KeyXform xf;
+  const uint32_t* bases;   // this pass's bases of row 0
+  int64_t bases_row_stride;
+  uint32_t* offsets;       // [rows * tiles_per_row][radix]: counts, then offsets
+};
+cudaError_t launch_tile_counts_f16(const TileCountArgs& a, cudaStream_t s);
+
+// A sort whose rows (one row for a flat sort) hold at most kSmallMaxKeys
+// keys: one CTA per row does every pass in shared memory, one launch.
+constexpr int64_t kSmallMaxKeys = 4096;
+struct SmallArgs {
+  const void* keys_in;
+  void* keys_out;
+  const void* vals_in;     // u32 payloads (kValU32) or unused
+  void* vals_out;          // u32 payloads, or int64 column indices (kValIdx)
+  int64_t rows, cols;
+  int begin_bit, passes;
+  uint32_t last_mask;
+  KeyXform xf;
+  uint32_t* header;        // scratch header: error word and passes run
+};
+bool small_sort_fits(KeyKind k, ValKind v, int bits, int64_t cols);
+cudaError_t launch_small(KeyKind k, ValKind v, int bits, const SmallArgs& a, cudaStream_t s);
 cudaError_t launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t s);
 // After the passes: when no pass ran (every pass was the identity) copy the
 // input to the output, and write column indices as the identity; when an

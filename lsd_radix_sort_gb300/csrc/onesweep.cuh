@@ -259,7 +259,8 @@ struct TileIo {
 
 // One tile: rank, publish, look back, stage, write.  Called by every thread
 // of the CTA; begins and ends with all threads converged.
-template <bool FULL, bool DYN, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
+template <bool FULL, bool DYN, bool PRE, class KeyOp, int BITS, int VK, int THREADS, int ITEMS,
+          int WIN>
 __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
                                            TileScratch<THREADS / kWarp, (1 << BITS)>& s,
                                            const TileIo<KeyOp>& io, uint32_t* status_row,
@@ -337,7 +338,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
       }
       my_count = (!FULL && tid == R - 1) ? total - static_cast<uint32_t>(TILE - valid) : total;
       // a partial tile is the last of its row: nothing waits on it
-      if (FULL) st_relaxed(status_tile + tid, (t == 0 ? kFlagP : kFlagA) | my_count);
+      if (FULL && !PRE) st_relaxed(status_tile + tid, (t == 0 ? kFlagP : kFlagA) | my_count);
     }
     uint32_t incl = total;
 #pragma unroll
@@ -403,7 +404,11 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   LSDRS_PHASE(3);  // staging (thread 0's share)
 
   // ---- 6. decoupled look-back -------------------------------------------
-  if (tid < R) {
+  // (PRE: the tile's output offsets were computed before the pass from
+  // per-tile digit counts, so there is nothing to wait for)
+  if (PRE && tid < R) {
+    s.g_off[tid] = a.offsets[(row * a.tiles_per_row + t) * R + tid] - start;
+  } else if (tid < R) {
     uint32_t excl = 0;
     if (t > 0) {
       excl = look_back<R, WIN>(status_row + tid, t, a.error, a.timeout_ns, trips, polls);
@@ -468,7 +473,8 @@ struct SweepSmem {
 // DYN: the schedule (which passes run, between which buffers) comes from
 // K-SCAN through the tile counter; otherwise it is the host's static one in
 // the kernel arguments (every pass runs).
-template <bool TAIL, bool DYN, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
+template <bool TAIL, bool DYN, bool PRE, class KeyOp, int BITS, int VK, int THREADS, int ITEMS,
+          int WIN>
 __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
   using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
   using T = typename KeyOp::T;
@@ -522,7 +528,7 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
   io.val_bar = nullptr;
   io.vals_in = false;
   if (s.abort) {  // an earlier tile failed: release successors and stop
-    if (!TAIL && tid < R) st_relaxed(status_row + t * R + tid, kFlagP);
+    if (!TAIL && !PRE && tid < R) st_relaxed(status_row + t * R + tid, kFlagP);
   } else {
     if (VK != kValNone && pb.template vals_in<VK>() != nullptr) {
       // Payloads are not needed before the staging step: a full tile with an
@@ -543,21 +549,24 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
         for (int i = tid; i < valid; i += THREADS) s.vals[i] = ld_stream(vsrc + i);
       }
     }
-    sweep_tile<!TAIL, DYN, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io, status_row, row, t,
+    sweep_tile<!TAIL, DYN, PRE, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io, status_row,
+                                                                   row, t,
                                                            tile_begin, valid);
   }
   uint32_t* zero = PassBufs<DYN>{DYN ? s.scratch.code : a.code, a}.status_zero();
-  if (!TAIL && zero != nullptr && tid < R) zero[static_cast<int64_t>(s.tile_id) * R + tid] = 0;
+  if (!TAIL && !PRE && zero != nullptr && tid < R)
+    zero[static_cast<int64_t>(s.tile_id) * R + tid] = 0;
 }
 
-template <bool DYN, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB, int WIN>
+template <bool DYN, bool PRE, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB,
+          int WIN>
 __global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
-  onesweep_body<false, DYN, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a);
+  onesweep_body<false, DYN, PRE, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a);
 }
 
-template <bool DYN, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
+template <bool DYN, bool PRE, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
 __global__ void __launch_bounds__(THREADS, 1) onesweep_tail_kernel(SweepArgs a) {
-  onesweep_body<true, DYN, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a);
+  onesweep_body<true, DYN, PRE, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a);
 }
 
 template <class K>
@@ -579,7 +588,9 @@ constexpr int kTailThreads = 1024;
 
 // One pass: the full tiles, then the partial tile of each row.  Returns
 // the number of kernels launched in *launched.
-template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB, int WIN>
+// PRE: offsets precomputed by the tile-count kernels (row-wise sorts only).
+template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB, int WIN,
+          bool PRE = false>
 cudaError_t launch_sweep_t(const SweepArgs& args, int* launched, cudaStream_t s) {
   using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
   constexpr int TILE = S::kTile;
@@ -593,9 +604,9 @@ cudaError_t launch_sweep_t(const SweepArgs& args, int* launched, cudaStream_t s)
   if (full > 0) {
     cudaError_t e =
         a.dynamic
-            ? launch_with_smem(onesweep_kernel<true, KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>,
+            ? launch_with_smem(onesweep_kernel<true, PRE, KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>,
                                static_cast<unsigned>(full), THREADS, sizeof(S), s, a)
-            : launch_with_smem(onesweep_kernel<false, KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>,
+            : launch_with_smem(onesweep_kernel<false, PRE, KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>,
                                static_cast<unsigned>(full), THREADS, sizeof(S), s, a);
     if (e != cudaSuccess) return e;
     ++*launched;
@@ -603,10 +614,10 @@ cudaError_t launch_sweep_t(const SweepArgs& args, int* launched, cudaStream_t s)
   if (a.rows > 0 && a.cols % TILE != 0) {
     cudaError_t e =
         a.dynamic
-            ? launch_with_smem(onesweep_tail_kernel<true, KeyOp, BITS, VK, kTailThreads,
+            ? launch_with_smem(onesweep_tail_kernel<true, PRE, KeyOp, BITS, VK, kTailThreads,
                                                     TAIL_ITEMS, WIN>,
                                static_cast<unsigned>(a.rows), kTailThreads, sizeof(ST), s, a)
-            : launch_with_smem(onesweep_tail_kernel<false, KeyOp, BITS, VK, kTailThreads,
+            : launch_with_smem(onesweep_tail_kernel<false, PRE, KeyOp, BITS, VK, kTailThreads,
                                                     TAIL_ITEMS, WIN>,
                                static_cast<unsigned>(a.rows), kTailThreads, sizeof(ST), s, a);
     if (e != cudaSuccess) return e;

@@ -5,7 +5,12 @@
 namespace lsdrs {
 
 cudaError_t launch_sweep_f16(const SweepArgs& a, int* launched, cudaStream_t s) {
-  return launch_sweep_t<KeyF16Bits, 8, kValIdx, kShapeF16Idx.threads, kShapeF16Idx.items, kShapeF16Idx.min_blocks, kShapeF16Idx.window>(a, launched, s);
+  constexpr SweepShape S = kShapeF16Idx;
+  if (a.offsets != nullptr)
+    return launch_sweep_t<KeyF16Bits, 8, kValIdx, S.threads, S.items, S.min_blocks, S.window,
+                          true>(a, launched, s);
+  return launch_sweep_t<KeyF16Bits, 8, kValIdx, S.threads, S.items, S.min_blocks, S.window>(
+      a, launched, s);
 }
 
 }  // namespace lsdrs

@@ -70,7 +70,9 @@ def test_skipped_passes_pairs(rs, case, in_place, n):
     ek, ev = oracle.sort(keys, vals, begin, end, bits)
     ko, vo, run = sort_pairs(rs, keys, vals, begin, end, bits, in_place)
     assert np.array_equal(ko, ek) and np.array_equal(vo, ev)
-    assert run == want_run
+    # up to 4,096 keys one kernel sorts the whole input in shared memory,
+    # every pass included
+    assert run == (want_run if n > 4096 else oracle.num_passes(begin, end, bits))
 
 
 @pytest.mark.parametrize("case", sorted(CASES))
