@@ -9,9 +9,11 @@
 // How one CTA computes it for a tile of THREADS * ITEMS consecutive keys:
 //  1. The tile index comes from an atomic counter, so tiles start in index
 //     order and every tile a CTA waits on belongs to a CTA that is already
-//     running (forward progress of the look-back).
+//     running (forward progress of the look-back).  With pass skipping the
+//     counter's top byte also carries the pass's schedule (which buffers it
+//     reads and writes, or that it is skipped), written there by K-SCAN.
 //  2. The tile's payloads are requested at once with one bulk (TMA) copy into
-//     shared memory; they are not needed before step 7.  Keys are loaded
+//     shared memory; they are not needed before step 5.  Keys are loaded
 //     warp-striped into registers: warp w owns a contiguous run of 32*ITEMS
 //     keys and its item i covers keys 32*i .. 32*i+31 of that run, one per
 //     lane, so (warp, item, lane) order is input order.
@@ -23,33 +25,34 @@
 //     (section 13.2's rank within digit), done for all digits at once.
 //  4. A per-digit scan over the warps gives each warp's offset and the
 //     tile's digit counts; the counts are published at once for later tiles
-//     (decoupled look-back, flag A), then a scan over the digits gives each
-//     digit's start inside the tile.
-//  5. Keys are placed in shared memory in tile-sorted order.
+//     (decoupled look-back, flag A), then a block-wide scan over the digits
+//     gives each digit's start inside the tile.
+//  5. Keys, then payloads, are placed in shared memory in tile-sorted order.
 //  6. Look-back: for each digit, the counts of earlier tiles of the row are
 //     summed walking backwards, a window of tiles per memory round trip,
 //     until a tile that has published its inclusive prefix (flag P); this
-//     tile then publishes its own inclusive prefix.  The precomputed
-//     alternative (per-tile offsets from a separate pass, FlagTree PR #1084
-//     section 2) needs a second read of the keys; the look-back needs none.
-//     Every wait is bounded in time.
+//     tile then publishes its own inclusive prefix.  Every wait is bounded
+//     in time.  Row-wise sorts may instead take offsets precomputed before
+//     the pass from per-tile counts (FlagTree PR #1084 section 2; tiles.cu),
+//     at the cost of a second read of the keys.
 //  7. Thread j writes staged key j to base[d] + prefix[d] + (j - start[d]):
 //     every digit's keys leave as one contiguous run ("100 Days of GPU",
 //     day 35: after the local sort the write out is one run per digit).
 //     Payloads follow through the same staging buffer.
-// Lanes past the end of the last tile take the highest digit, rank after
-// every real key of the tile, are not counted in the published counts and
-// are not stored (the page's sentinel padding, without the padding).  Full
-// tiles run a separate instantiation with no bounds checks.
+// The last, partial tile of each row runs in a separate tail kernel after
+// the full tiles (nothing in the row waits on it), so the full-tile kernel
+// has no bounds checks.  In the tail, lanes past the end of the row take the
+// highest digit, rank after every real key of the tile, are not counted in
+// the published counts and are not stored (the page's sentinel padding,
+// without the padding).
 #pragma once
 #include "common.cuh"
 #include "kernels.h"
 #include "keys.cuh"
 
 // Tuning knobs (build-time): a sleep between polls of a word that is not
-// ready, the hardware
-// match instruction instead of per-bit ballots, the bulk copy of payloads,
-// and look-back statistics for measurement builds.
+// ready, the hardware match instruction instead of per-bit ballots, the bulk
+// copy of payloads, and look-back statistics for measurement builds.
 #ifndef LSDRS_SPIN_SLEEP_NS
 #define LSDRS_SPIN_SLEEP_NS 0
 #endif
