@@ -38,9 +38,13 @@ struct HistCfg {
 
 // Per-thread view of the counters: shift and mask of every pass held in
 // registers; ALL = every pass of the key type is present (the usual case),
-// which drops the per-pass bound test.
-template <class KeyOp, int BITS, bool ALL>
+// which drops the per-pass bound test.  BYTES = 8-bit digits covering the
+// whole key from bit 0, so that pass p's digit is byte p of T(k): the key is
+// transformed once and each digit is one byte permute, which keeps the
+// counting loop short enough to run at the speed of the key reads.
+template <class KeyOp, int BITS, bool ALL, bool BYTES = false>
 struct KeyCounter {
+  static_assert(!BYTES || (ALL && BITS == 8), "byte digits cover every pass");
   using Cfg = HistCfg<KeyOp, BITS>;
   static constexpr int R = Cfg::kRadix;
   static constexpr int C = Cfg::kCols;
@@ -66,7 +70,15 @@ struct KeyCounter {
     }
   }
   __device__ __forceinline__ void add(typename KeyOp::T k) const {
-    if constexpr (kHeld) {
+    if constexpr (BYTES) {
+      const auto t = KeyOp::encode(k, xf);
+#pragma unroll
+      for (int p = 0; p < MP; ++p) {
+        const uint32_t w = static_cast<uint32_t>(t >> (32 * (p / 4)));
+        const uint32_t d = __byte_perm(w, 0u, 0x4440u + (p & 3));
+        atomicAdd(col + (p * R + d) * C, 1u);
+      }
+    } else if constexpr (kHeld) {
 #pragma unroll
       for (int p = 0; p < MP; ++p) {
         if (ALL || p < passes) {
@@ -87,9 +99,10 @@ struct KeyCounter {
 // Counts keys [begin, end) of one row slice: a scalar head up to 16-byte
 // alignment, a vectorised body (U 16-byte loads in flight per thread) and a
 // scalar tail.
-template <class KeyOp, int BITS, bool ALL>
+template <class KeyOp, int BITS, bool ALL, bool BYTES>
 __device__ __forceinline__ void count_range(const typename KeyOp::T* base, int64_t begin,
-                                            int64_t end, const KeyCounter<KeyOp, BITS, ALL>& c) {
+                                            int64_t end,
+                                            const KeyCounter<KeyOp, BITS, ALL, BYTES>& c) {
   using T = typename KeyOp::T;
   using Cfg = HistCfg<KeyOp, BITS>;
   constexpr int V = Cfg::kVec;
@@ -152,12 +165,16 @@ __global__ void __launch_bounds__(kHistThreads, 1) upfront_hist_kernel(HistArgs 
   const T* base = static_cast<const T*>(a.keys) + row * a.cols;
   uint32_t* col = cnt + (tid & (C - 1));
   if (begin < end) {
-    if (a.passes == Cfg::kMaxPasses) {
+    if (BITS == 8 && a.passes == Cfg::kMaxPasses && a.begin_bit == 0 && a.last_mask == 0xFFu) {
+      const KeyCounter<KeyOp, BITS, true, BITS == 8> c(col, a.begin_bit, a.passes, a.last_mask,
+                                                       a.xf);
+      count_range(base, begin, end, c);
+    } else if (a.passes == Cfg::kMaxPasses) {
       const KeyCounter<KeyOp, BITS, true> c(col, a.begin_bit, a.passes, a.last_mask, a.xf);
-      count_range<KeyOp, BITS, true>(base, begin, end, c);
+      count_range(base, begin, end, c);
     } else {
       const KeyCounter<KeyOp, BITS, false> c(col, a.begin_bit, a.passes, a.last_mask, a.xf);
-      count_range<KeyOp, BITS, false>(base, begin, end, c);
+      count_range(base, begin, end, c);
     }
   }
   __syncthreads();

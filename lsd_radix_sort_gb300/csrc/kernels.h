@@ -86,7 +86,13 @@ constexpr SweepShape sweep_shape(KeyKind k, ValKind v) {
 }
 
 constexpr int kHistThreads = 1024;
-constexpr int kHistTargetCtas = 608;   // 152 SMs x 4 resident CTAs
+// K-HIST grid: one 1,024-thread CTA fits an SM (its counters take up to
+// 128 KB of shared memory), so a flat sort takes one wave, one CTA per SM
+// (152 SMs): no wave tail, and K-SCAN adds 152 partial counts per digit.
+#ifndef LSDRS_HIST_CTAS
+#define LSDRS_HIST_CTAS 152
+#endif
+constexpr int kHistTargetCtas = LSDRS_HIST_CTAS;
 constexpr int64_t kHistMinChunk = 4096;
 constexpr int kScanThreads = 256;
 

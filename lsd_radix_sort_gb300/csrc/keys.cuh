@@ -16,7 +16,8 @@
 // layout (FlagTree PR #1084 folds the descending flag into the key
 // conversion of every load).  T is applied on the fly at every digit
 // extraction and never stored: the stored bits are carried unchanged, so no
-// inverse is needed on the way out.
+// inverse is needed on the way out.  encode() gives T(k) whole, for callers
+// that take several digits of one key (the upfront histogram).
 #pragma once
 #include <cstdint>
 
@@ -28,6 +29,7 @@ namespace lsdrs {
 struct KeyU32 {
   using T = uint32_t;
   static constexpr int kBits = 32;
+  __device__ __forceinline__ static uint32_t encode(T k, const KeyXform&) { return k; }
   __device__ __forceinline__ static uint32_t digit(T k, int shift, uint32_t mask,
                                                    const KeyXform&) {
     return (k >> shift) & mask;
@@ -38,6 +40,10 @@ struct KeyU32 {
 struct KeyX32 {
   using T = uint32_t;
   static constexpr int kBits = 32;
+  __device__ __forceinline__ static uint32_t encode(T k, const KeyXform& x) {
+    return k ^ (static_cast<int32_t>(k) < 0 ? static_cast<uint32_t>(x.neg)
+                                            : static_cast<uint32_t>(x.pos));
+  }
   __device__ __forceinline__ static uint32_t digit(T k, int shift, uint32_t mask,
                                                    const KeyXform& x) {
     const uint32_t t = k ^ (static_cast<int32_t>(k) < 0 ? static_cast<uint32_t>(x.neg)
@@ -49,6 +55,7 @@ struct KeyX32 {
 struct KeyU64 {
   using T = uint64_t;
   static constexpr int kBits = 64;
+  __device__ __forceinline__ static uint64_t encode(T k, const KeyXform&) { return k; }
   __device__ __forceinline__ static uint32_t digit(T k, int shift, uint32_t mask,
                                                    const KeyXform&) {
     return static_cast<uint32_t>(k >> shift) & mask;
@@ -58,6 +65,9 @@ struct KeyU64 {
 struct KeyX64 {
   using T = uint64_t;
   static constexpr int kBits = 64;
+  __device__ __forceinline__ static uint64_t encode(T k, const KeyXform& x) {
+    return k ^ (static_cast<int64_t>(k) < 0 ? x.neg : x.pos);
+  }
   __device__ __forceinline__ static uint32_t digit(T k, int shift, uint32_t mask,
                                                    const KeyXform& x) {
     const uint64_t t = k ^ (static_cast<int64_t>(k) < 0 ? x.neg : x.pos);
@@ -69,6 +79,11 @@ struct KeyX64 {
 struct KeyF16Bits {
   using T = uint16_t;
   static constexpr int kBits = 16;
+  // T(k) in the low 16 bits (the bits above are not part of the key)
+  __device__ __forceinline__ static uint32_t encode(T k, const KeyXform& x) {
+    const uint32_t u = k;
+    return u ^ ((u & 0x8000u) ? static_cast<uint32_t>(x.neg) : static_cast<uint32_t>(x.pos));
+  }
   __device__ __forceinline__ static uint32_t digit(T k, int shift, uint32_t mask,
                                                    const KeyXform& x) {
     const uint32_t u = k;
