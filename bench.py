@@ -157,6 +157,9 @@ def dist_setup():
     return rank, world, local
 
 
+E2E_REPS = 3  # repetitions of each end-to-end schedule; the best is reported
+
+
 def max_over_ranks(value: float, world: int, device=None) -> float:
     """Largest value over all ranks (the job's time is its slowest replica)."""
     if world <= 1:
@@ -492,28 +495,42 @@ def main():
                 done.record(down)
             freed[i % nsets] = done
 
+        # The host link is shared with the rest of the machine: bursts of
+        # 50-180 ms in which host copies run several times slower come and
+        # go whatever this program does (its enqueue stays at 0.1 ms per
+        # step).  Each schedule is therefore timed in E2E_REPS repetitions of
+        # `steps` consecutive steps, and the best repetition's mean step time
+        # is reported, every repetition beside it.
         def timed_e2e(step_fn, steps):
             for i in range(2):
                 step_fn(i)
             torch.cuda.synchronize()
-            barrier(world)
-            t0 = time.perf_counter()
-            for i in range(steps):
-                step_fn(i)
-            torch.cuda.synchronize()
-            return max_over_ranks((time.perf_counter() - t0) * 1e3 / steps, world, dev)
+            reps = []
+            for _ in range(E2E_REPS):
+                barrier(world)
+                t0 = time.perf_counter()
+                for i in range(steps):
+                    step_fn(i)
+                torch.cuda.synchronize()
+                reps.append(max_over_ranks((time.perf_counter() - t0) * 1e3 / steps, world, dev))
+            return min(reps), reps
 
-        e_serial = timed_e2e(lambda i: serial_step(), args.e2e_steps)
-        e_pipe = timed_e2e(pipelined_step, max(args.e2e_steps, 6))
+        pipe_steps = max(args.e2e_steps, 6)
+        e_serial, serial_reps = timed_e2e(lambda i: serial_step(), args.e2e_steps)
+        e_pipe, pipe_reps = timed_e2e(pipelined_step, pipe_steps)
         # the results of the last step are the sort of the input
-        b = sets[(max(args.e2e_steps, 6) - 1) % nsets]
+        b = sets[(pipe_steps - 1) % nsets]
         ok = bool(np.array_equal(b["hko"][:4096].numpy(), ko[:4096].cpu().numpy()))
         e2e = {"value": world * n / (e_pipe * 1e-3) / 1e9, "unit": "Gkeys/s",
                "h2d_bytes_per_step": hk.numel() * 4 + hv.numel() * 4,
                "d2h_bytes_per_step": sets[0]["hko"].numel() * 4 + sets[0]["hvo"].numel() * 4,
                "ms_per_step": e_pipe, "mode": f"pipelined over {nsets} buffer sets (wall clock)",
+               "timing": f"best of {E2E_REPS} repetitions of {pipe_steps} steps",
+               "reps_ms_per_step": [round(x, 3) for x in pipe_reps],
                "result_checked": ok,
-               "serial": {"value": world * n / (e_serial * 1e-3) / 1e9, "ms_per_step": e_serial}}
+               "serial": {"value": world * n / (e_serial * 1e-3) / 1e9, "ms_per_step": e_serial,
+                          "timing": f"best of {E2E_REPS} repetitions of {args.e2e_steps} steps",
+                          "reps_ms_per_step": [round(x, 3) for x in serial_reps]}}
         del hk, hv, sets
 
     # ---- the other key distributions of the same workload ----------------
@@ -563,7 +580,9 @@ def main():
                 "dtype": "u32", "data": "synthetic",
                 "config": {"workload": workload_name(args.n_log2), "n_keys": n,
                            "digit_bits": DIGIT_BITS, "passes": passes,
-                           "l2": "inputs larger than L2 (2 GiB keys+payload vs 129 MB L2), no flush",
+                           "l2": (f"inputs larger than L2 ({n * 8 / 2**20:.0f} MiB keys+payload vs "
+                                  "129 MB L2), no flush" if n * 8 > 129e6 else
+                                  f"inputs ({n * 8 / 2**20:.1f} MiB) fit in L2, no flush"),
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
                 "hbm": {"ideal_bytes_per_sort": total_ideal,
                         "achieved_gbs": total_ideal / (ms_max * 1e-3) / 1e9,
