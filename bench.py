@@ -515,6 +515,29 @@ def main():
                 reps.append(max_over_ranks((time.perf_counter() - t0) * 1e3 / steps, world, dev))
             return min(reps), reps
 
+        # The host link on its own: one 1 GiB copy each way, then both at once
+        # (the pipelined schedule's bound), best of three.
+        def link_gbs(fn, nbytes):
+            best = None
+            for _ in range(3):
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                fn()
+                torch.cuda.synchronize()
+                dt = time.perf_counter() - t0
+                best = dt if best is None else min(best, dt)
+            return nbytes / best / 1e9
+
+        def both_ways():
+            with torch.cuda.stream(up):
+                sets[0]["dk"].copy_(hk, non_blocking=True)
+            with torch.cuda.stream(down):
+                sets[0]["hko"].copy_(sets[1]["dk"], non_blocking=True)
+
+        link = {"h2d_gbs": link_gbs(lambda: sets[0]["dk"].copy_(hk, non_blocking=True), hk.numel() * 4),
+                "d2h_gbs": link_gbs(lambda: sets[0]["hko"].copy_(sets[0]["dk"], non_blocking=True),
+                                    hk.numel() * 4),
+                "both_ways_gbs": link_gbs(both_ways, 2 * hk.numel() * 4)}
         pipe_steps = max(args.e2e_steps, 6)
         e_serial, serial_reps = timed_e2e(lambda i: serial_step(), args.e2e_steps)
         e_pipe, pipe_reps = timed_e2e(pipelined_step, pipe_steps)
@@ -528,6 +551,7 @@ def main():
                "timing": f"best of {E2E_REPS} repetitions of {pipe_steps} steps",
                "reps_ms_per_step": [round(x, 3) for x in pipe_reps],
                "result_checked": ok,
+               "host_link": {k: round(v, 1) for k, v in link.items()},
                "serial": {"value": world * n / (e_serial * 1e-3) / 1e9, "ms_per_step": e_serial,
                           "timing": f"best of {E2E_REPS} repetitions of {args.e2e_steps} steps",
                           "reps_ms_per_step": [round(x, 3) for x in serial_reps]}}
