@@ -224,6 +224,64 @@ def small_sort_latency(rs, torch, workloads, log2_sizes, reps: int = 200):
     return out
 
 
+def keys_only_configs(rs, torch, workloads, reps: int = 50):
+    """The two keys-only workloads: 1,024 keys below 4,096 sorted on bits
+    0-11 in three 4-bit passes, and 4,194,304 uniform u32 keys sorted in
+    eight 4-bit or four 8-bit passes (seeds 0-2; the inputs fit in L2).
+    Stream-launched time per sort, and the CUDA-graph replay of the same
+    call, with each result checked against a stable sort on the device."""
+    import numpy as np
+    stream = torch.cuda.current_stream()
+    cases = [("1024_keys_b4_bits0_12", 1024, 4, 12, lambda seed: workloads.u32_small(1024, seed, 12)),
+             ("2^22_keys_b4", 1 << 22, 4, 32, lambda seed: workloads.u32_uniform(1 << 22, seed)),
+             ("2^22_keys_b8", 1 << 22, 8, 32, lambda seed: workloads.u32_uniform(1 << 22, seed))]
+    out = {}
+    for name, n, bits, end, gen in cases:
+        per_seed = []
+        for seed in range(3):
+            dk = torch.from_numpy(gen(seed).view(np.int32)).cuda()
+            ko = torch.empty_like(dk)
+            temp = torch.empty(rs.temp_bytes(n, 4, 0, 0, end, bits), dtype=torch.uint8,
+                               device="cuda")
+
+            def sort():
+                rs.radix_sort_keys(dk, ko, 0, end, bits, temp=temp)
+
+            def timed(fn):
+                for _ in range(5):
+                    fn()
+                torch.cuda.synchronize()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(reps):
+                    fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                return a.elapsed_time(b) * 1e3 / reps
+            t_stream = timed(sort)
+            side = torch.cuda.Stream()
+            side.wait_stream(stream)
+            with torch.cuda.stream(side):
+                for _ in range(3):
+                    sort()
+            stream.wait_stream(side)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                sort()
+            t_graph = timed(g.replay)
+            k64 = dk.to(torch.int64) & 0xFFFFFFFF
+            want = torch.sort(k64 & ((1 << end) - 1), stable=True)
+            ok = bool(torch.equal(ko.to(torch.int64) & 0xFFFFFFFF, k64[want.indices]))
+            per_seed.append({"seed": seed, "stream_us": round(t_stream, 2),
+                             "graph_us": round(t_graph, 2), "checked": ok})
+            del g, dk, ko, temp
+        best = min(min(r["stream_us"], r["graph_us"]) for r in per_seed)
+        out[name] = {"n": n, "digit_bits": bits, "passes": (end + bits - 1) // bits,
+                     "gkeys_s_best": round(n / best / 1e3, 2), "seeds": per_seed}
+    return out
+
+
 ROW_SHAPES = [(64, 64), (256, 256), (1024, 1024), (4096, 4096), (1024, 65536), (1024, 1),
               (1024, 512), (16, 131072), (8, 262144)]
 
@@ -583,8 +641,10 @@ def main():
                 rs.set_pass_skipping(False)
 
     small = None
+    keys_cfg = None
     if not args.no_small_sorts:
-        small = small_sort_latency(rs, torch, workloads, (10, 12, 14, 16, 18, 20))
+        small = small_sort_latency(rs, torch, workloads, (10, 12, 13, 14, 16, 18, 20))
+        keys_cfg = keys_only_configs(rs, torch, workloads)
     rows_tab = None
     if not args.no_rows:
         rows_tab = row_sorts(rs, torch, workloads)
@@ -613,7 +673,8 @@ def main():
                         "frac_of_peak": total_ideal / (ms_max * 1e-3) / 1e9 / peak},
                 "e2e": e2e, "gpu_launches": launches, "kernels": kernels,
                 "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks,
-                "distributions": dists, "small_sorts": small, "row_sorts": rows_tab}
+                "distributions": dists, "small_sorts": small, "keys_only_configs": keys_cfg,
+                "row_sorts": rows_tab}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

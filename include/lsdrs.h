@@ -185,7 +185,6 @@ rs_status radix_sort_histograms(const void* keys, int key_bytes, size_t n,
  * that used `temp` (RS_OK or RS_ERR_LOOKBACK_TIMEOUT), or RS_ERR_CUDA. */
 rs_status radix_sort_device_status(const void* temp, void* stream);
 
-/* Human-readable name of a status code (static storage). */
 /* Pass skipping, for every sort enqueued after the call (process-wide;
  * default off).  With it on, a pass in which every key (every key of every
  * row, for a row-wise sort) has the same digit is the identity permutation
@@ -214,6 +213,20 @@ rs_status rs_set_tile_offsets(int precomputed);
  *   passes  (host) receives the count (0 .. passes of the bit range) */
 rs_status radix_sort_passes_run(const void* temp, int* passes, void* stream);
 
+/* The one-kernel path for short rows, for every sort enqueued after the call
+ * (process-wide; default on).  With it on, a sort whose rows (the whole
+ * input, for a flat sort) hold at most 8,192 keys, with 4- or 8-bit digits,
+ * runs in one kernel: one CTA per row loads the row into shared memory,
+ * does every pass there (rank, digit scan, scatter within the row, which is
+ * a single tile: CUDA Handbook ch. 16, Listing 16-8, on one tile) and
+ * writes the sorted row once.  Off: such sorts take the multi-kernel path
+ * (K-HIST, K-SCAN, one scatter kernel per pass) like longer rows.  The
+ * results are identical; the multi-kernel path then also runs every pass
+ * that pass skipping does not remove, which the one-kernel path never skips.
+ *   on   0 or 1 (anything else: RS_ERR_INVALID) */
+rs_status rs_set_small_sort(int on);
+
+/* Human-readable name of a status code (static storage). */
 const char* rs_status_string(rs_status status);
 
 /* Limit in nanoseconds on one look-back wait inside the scatter kernels

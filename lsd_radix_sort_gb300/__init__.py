@@ -23,7 +23,8 @@ from . import build as _build
 __all__ = [
     "RadixSortError", "load_library", "library_path", "temp_bytes", "radix_sort_keys",
     "radix_sort_pairs", "segmented_sort", "segmented_temp_bytes", "upfront_histograms",
-    "device_status", "passes_run", "set_pass_skipping", "set_tile_offsets", "copy_probe", "set_lookback_timeout_ns", "lookback_timeout_probe",
+    "device_status", "passes_run", "set_pass_skipping", "set_tile_offsets", "set_small_sort",
+    "SMALL_SORT_MAX_KEYS", "copy_probe", "set_lookback_timeout_ns", "lookback_timeout_probe",
     "profile_enable", "profile_read", "launch_count_reset", "EXPORTED_SYMBOLS",
 ]
 
@@ -32,6 +33,10 @@ RS_F16, RS_BF16 = 0, 1
 KEY_TYPES = {"u32": (0, 4), "i32": (1, 4), "f32": (2, 4), "u64": (3, 8), "i64": (4, 8),
              "f64": (5, 8)}
 RS_MAX_KEYS = (1 << 30) - 1
+# Rows (or flat inputs) of at most this many keys, with 4- or 8-bit digits,
+# are sorted by one kernel that runs every pass in shared memory (unless
+# set_small_sort(False)); it runs every pass, pass skipping included.
+SMALL_SORT_MAX_KEYS = 8192
 KERNEL_NAMES = {0: "upfront_hist", 1: "digit_scan", 2: "onesweep", 3: "copy_probe",
                 4: "timeout_probe", 5: "finish", 6: "tile_counts",
                 7: "small_sort"}
@@ -43,7 +48,7 @@ EXPORTED_SYMBOLS = (
     "rs_status_string", "rs_set_lookback_timeout_ns", "rs_lookback_timeout_probe",
     "rs_copy_probe", "rs_profile_enable", "rs_profile_read", "rs_launch_count_reset",
     "radix_sort_pairs_u32_noalloc", "radix_sort_keys_typed", "radix_sort_pairs_typed",
-    "radix_sort_passes_run", "rs_set_pass_skipping", "rs_set_tile_offsets",
+    "radix_sort_passes_run", "rs_set_pass_skipping", "rs_set_tile_offsets", "rs_set_small_sort",
 )
 
 
@@ -104,6 +109,7 @@ def load_library() -> ctypes.CDLL:
             "radix_sort_passes_run": [P, P, P],
             "rs_set_pass_skipping": [i],
             "rs_set_tile_offsets": [i],
+            "rs_set_small_sort": [i],
             "radix_sort_pairs_typed": [i, i, P, P, P, P, sz, i, i, i, P, sz, P],
         }
         for name, args in sig.items():
@@ -323,6 +329,12 @@ def set_pass_skipping(on: bool):
     """Skip identity passes (every key with the same digit) from now on
     (process-wide; off by default)."""
     _check(load_library().rs_set_pass_skipping(int(bool(on))), "rs_set_pass_skipping")
+
+
+def set_small_sort(on: bool):
+    """Sort rows of at most SMALL_SORT_MAX_KEYS keys in one kernel from now
+    on (process-wide; on by default); off, they take the multi-kernel path."""
+    _check(load_library().rs_set_small_sort(int(bool(on))), "rs_set_small_sort")
 
 
 def passes_run(temp, stream=None) -> int:

@@ -16,6 +16,7 @@ namespace {
 std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_pass_skipping{0};
+std::atomic<int> g_small_sort{1};
 std::atomic<int> g_tile_offsets{0};
 
 // ---------------------------------------------------------------- profiling
@@ -237,7 +238,8 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
   if (p.val == kValIdx && p.passes > 2) return RS_ERR_INVALID;  // 16-bit keys: two passes
 
   // rows of at most one small tile: the whole sort in one kernel
-  if (small_sort_fits(p.key, p.val, p.bits, p.cols)) {
+  if (g_small_sort.load(std::memory_order_relaxed) != 0 &&
+      small_sort_fits(p.key, p.val, p.bits, p.cols)) {
     SmallArgs sa{};
     sa.keys_in = keys_in;
     sa.keys_out = keys_out;
@@ -541,6 +543,12 @@ const char* rs_status_string(rs_status status) {
 rs_status rs_set_pass_skipping(int on) {
   if (on != 0 && on != 1) return RS_ERR_INVALID;
   g_pass_skipping.store(on, std::memory_order_relaxed);
+  return RS_OK;
+}
+
+rs_status rs_set_small_sort(int on) {
+  if (on != 0 && on != 1) return RS_ERR_INVALID;
+  g_small_sort.store(on, std::memory_order_relaxed);
   return RS_OK;
 }
 

@@ -227,7 +227,7 @@ cudaError_t launch_tile_counts_f16(const TileCountArgs& a, cudaStream_t s);
 
 // A sort whose rows (one row for a flat sort) hold at most kSmallMaxKeys
 // keys: one CTA per row does every pass in shared memory, one launch.
-constexpr int64_t kSmallMaxKeys = 4096;
+constexpr int64_t kSmallMaxKeys = 8192;
 struct SmallArgs {
   const void* keys_in;
   void* keys_out;

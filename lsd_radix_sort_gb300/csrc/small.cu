@@ -157,11 +157,13 @@ cudaError_t launch_small_t(const SmallArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// Two tile sizes: 1,024 keys (256 threads x 4) and 4,096 (512 x 8).
+// Three tile sizes: 1,024 keys (256 threads x 4), 4,096 (512 x 8) and 8,192
+// (1,024 x 8; more items per thread would not fit the registers).
 template <class KeyOp, int BITS, int VK>
 cudaError_t launch_small_b(const SmallArgs& a, cudaStream_t s) {
   if (a.cols <= 1024) return launch_small_t<KeyOp, BITS, VK, 256, 4>(a, s);
-  return launch_small_t<KeyOp, BITS, VK, 512, 8>(a, s);
+  if (a.cols <= 4096) return launch_small_t<KeyOp, BITS, VK, 512, 8>(a, s);
+  return launch_small_t<KeyOp, BITS, VK, 1024, 8>(a, s);
 }
 
 template <class KeyOp, int VK>

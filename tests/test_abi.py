@@ -119,6 +119,11 @@ def test_sort_calls_validate_before_launch(lib):
     assert lib.rs_copy_probe(bogus, temp, 15, None) == 1
     assert lib.rs_set_lookback_timeout_ns(0) == 1
     assert lib.rs_set_lookback_timeout_ns(2_000_000_000) == 0
+    # process-wide switches take 0 or 1 (restored to their defaults)
+    for name, default in (("rs_set_pass_skipping", 0), ("rs_set_tile_offsets", 0),
+                          ("rs_set_small_sort", 1)):
+        assert getattr(lib, name)(2) == 1 and getattr(lib, name)(-1) == 1
+        assert getattr(lib, name)(1 - default) == 0 and getattr(lib, name)(default) == 0
 
 
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):

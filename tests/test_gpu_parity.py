@@ -98,8 +98,18 @@ RAGGED = [1, 2, 31, 32, 33, 1000, TILE_U64 - 1, TILE_U64, TILE_U64 + 1, TILE_U64
           3 * TILE_U32_KEYS + 17, 100_003]
 
 
+@pytest.fixture(params=[True, False], ids=["one_kernel_short_rows", "multi_kernel_only"])
+def short_rows_one_kernel(rs, request):
+    """Inputs of at most rs.SMALL_SORT_MAX_KEYS keys are sorted by one kernel;
+    with it off the tile-boundary sizes below exercise the scatter and tail
+    kernels instead."""
+    rs.set_small_sort(request.param)
+    yield request.param
+    rs.set_small_sort(True)
+
+
 @pytest.mark.parametrize("n", RAGGED)
-def test_ragged_sizes(rs, n):
+def test_ragged_sizes(rs, n, short_rows_one_kernel):
     keys = workloads.u32_uniform(n, 11)
     keys[::3] = keys[0]  # ties across tiles
     vals = workloads.index_payload(n)
@@ -221,7 +231,8 @@ def test_segmented_page_shape(rs, kind, descending):
     assert np.array_equal(to_host(d.view(torch.int16), np.uint16), x), "input was written"
 
 
-@pytest.mark.parametrize("shape", [(1, 1), (3, 1000), (64, 64), (7, 4097), (2, 200_001),
+@pytest.mark.parametrize("shape", [(1, 1), (3, 1000), (64, 64), (7, 4097), (3, 8192), (3, 8193),
+                                   (2, 200_001),
                                    (16, 131072), (1024, 1), (5, 0), (0, 7)])
 @pytest.mark.parametrize("descending", [False, True])
 def test_segmented_shapes(rs, shape, descending):

@@ -62,7 +62,7 @@ CASES = {
 
 @pytest.mark.parametrize("case", sorted(CASES))
 @pytest.mark.parametrize("in_place", [False, True])
-@pytest.mark.parametrize("n", [1000, 5889, 300_001])
+@pytest.mark.parametrize("n", [1000, 5889, 9001, 300_001])
 def test_skipped_passes_pairs(rs, case, in_place, n):
     make, begin, end, bits, want_run = CASES[case]
     keys = make(n)
@@ -70,9 +70,9 @@ def test_skipped_passes_pairs(rs, case, in_place, n):
     ek, ev = oracle.sort(keys, vals, begin, end, bits)
     ko, vo, run = sort_pairs(rs, keys, vals, begin, end, bits, in_place)
     assert np.array_equal(ko, ek) and np.array_equal(vo, ev)
-    # up to 4,096 keys one kernel sorts the whole input in shared memory,
-    # every pass included
-    assert run == (want_run if n > 4096 else oracle.num_passes(begin, end, bits))
+    # short inputs are sorted by one kernel in shared memory, every pass
+    # included
+    assert run == (want_run if n > rs.SMALL_SORT_MAX_KEYS else oracle.num_passes(begin, end, bits))
 
 
 @pytest.mark.parametrize("case", sorted(CASES))

@@ -1,5 +1,5 @@
-"""Sorts of at most 4,096 keys per row run in one kernel (every pass in one
-CTA's shared memory): parity with the oracle at and around the two small
+"""Sorts of at most 8,192 keys per row run in one kernel (every pass in one
+CTA's shared memory): parity with the oracle at and around the three small
 tile sizes, for every key kind, both payload kinds, 4- and 8-bit digits,
 partial bit ranges, in place, and rows."""
 import numpy as np
@@ -13,7 +13,7 @@ from tests.test_gpu_typed import same_bits, typed_keys
 
 pytestmark = pytest.mark.gpu
 
-SMALL = [1, 2, 31, 32, 33, 255, 1023, 1024, 1025, 2049, 4095, 4096]
+SMALL = [1, 2, 31, 32, 33, 255, 1023, 1024, 1025, 2049, 4095, 4096, 4097, 6001, 8191, 8192]
 
 
 @pytest.mark.parametrize("n", SMALL)
@@ -35,7 +35,7 @@ def test_small_u32_u64(rs, n, bits):
 
 
 @pytest.mark.parametrize("key_type", ["i32", "f32", "i64", "f64"])
-@pytest.mark.parametrize("n", [7, 1024, 3001])
+@pytest.mark.parametrize("n", [7, 1024, 3001, 7777])
 def test_small_typed(rs, key_type, n):
     keys = typed_keys(key_type, n, 90 + n)
     vals = workloads.index_payload(n)
@@ -57,7 +57,8 @@ def test_small_in_place(rs):
     assert np.array_equal(to_host(dk, np.uint32), ek) and np.array_equal(to_host(dv, np.uint32), ev)
 
 
-@pytest.mark.parametrize("shape", [(1, 1), (3, 17), (100, 1024), (7, 4096), (2, 4095)])
+@pytest.mark.parametrize("shape", [(1, 1), (3, 17), (100, 1024), (7, 4096), (2, 4095), (5, 4097),
+                                   (3, 8192), (200, 6000)])
 def test_small_rows(rs, shape):
     h = workloads.rows16(*shape, "f16", seed=shape[1])
     x = torch.from_numpy(h.view(np.int16)).cuda().view(torch.float16)
@@ -66,3 +67,22 @@ def test_small_rows(rs, shape):
         ev, ei = oracle.segmented_sort16(h, descending)
         assert np.array_equal(v.view(torch.int16).cpu().numpy().view(np.uint16), ev)
         assert np.array_equal(i.cpu().numpy(), ei)
+
+
+def test_small_sort_switch(rs):
+    """With the one-kernel path off, the same short inputs take the
+    multi-kernel path and give the same results."""
+    n = 6001
+    keys = workloads.u32_uniform(n, 17)
+    vals = workloads.index_payload(n)
+    ek, ev = oracle.sort(keys, vals, 0, 32, 8)
+    try:
+        for on in (False, True):
+            rs.set_small_sort(on)
+            dk, dv = to_dev(keys), to_dev(vals)
+            ko, vo = poisoned_like(dk), poisoned_like(dv)
+            rs.radix_sort_pairs(dk, dv, ko, vo, 0, 32, 8)
+            assert np.array_equal(to_host(ko, np.uint32), ek)
+            assert np.array_equal(to_host(vo, np.uint32), ev)
+    finally:
+        rs.set_small_sort(True)
