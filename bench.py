@@ -282,6 +282,135 @@ def keys_only_configs(rs, torch, workloads, reps: int = 50):
     return out
 
 
+def _order_key(torch, k, key_type: str, descending: bool = False):
+    """int64 tensor whose signed order is the sort order of the keys (the
+    order-preserving transform of the typed sorts), for result checks."""
+    if key_type in ("u32", "i32", "f32"):
+        u = k.view(torch.int32).to(torch.int64) & 0xFFFFFFFF
+        top = u >> 31
+        if key_type == "i32":
+            t = u ^ 0x80000000
+        elif key_type == "f32":
+            t = torch.where(top == 1, u ^ 0xFFFFFFFF, u ^ 0x80000000)
+        else:
+            t = u
+        return (0xFFFFFFFF - t) if descending else t
+    x = k.view(torch.int64)
+    return (x ^ -(1 << 63)) if key_type == "u64" else x  # unsigned order as signed
+
+
+def _check_sorted_pairs(torch, keys_in, keys_out, vals_out, order_in, order_out) -> bool:
+    """Payload indices are a permutation carrying each key, keys are in order
+    and equal keys keep input order (the stable order is then fixed)."""
+    idx = vals_out.view(torch.int32).to(torch.int64)
+    if not torch.equal(keys_in[idx], keys_out):
+        return False
+    if bool((order_out[1:] < order_out[:-1]).any()):
+        return False
+    ties = order_out[1:] == order_out[:-1]
+    if bool((ties & (idx[1:] < idx[:-1])).any()):
+        return False
+    return bool(torch.bincount(idx, minlength=idx.numel()).eq(1).all())
+
+
+def config_sorts(rs, torch, workloads, n_log2: int, peak: float, reps: int = 10):
+    """The other headline-size workloads, each timed with CUDA events over
+    `reps` sorts after 3 warm-ups (inputs resident, larger than L2) and its
+    result checked on the device: u32 keys only; u64 key-value sorts
+    (uniform, skewed, the 0-39-bit run); typed 32-bit key-value sorts; the
+    row-wise fp16/bf16 sort of (1024, 65536) ascending and descending."""
+    import numpy as np
+    n = 1 << n_log2
+    stream = torch.cuda.current_stream()
+    out = {}
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    def entry(ms, nkeys, ideal, ok, **kw):
+        d = {"ms": round(ms, 4), "gkeys_s": round(nkeys / ms / 1e6, 2),
+             "ideal_bytes": ideal, "hbm_frac": round(ideal / (ms * 1e-3) / 1e9 / peak, 4),
+             "checked": ok}
+        d.update(kw)
+        return d
+
+    # u32 keys only: histogram read 4 B + 4 passes x (read + write) 4 B
+    k32 = torch.from_numpy(workloads.u32_uniform(n, 0).view(np.int32)).cuda()
+    ko = torch.empty_like(k32)
+    temp = torch.empty(rs.temp_bytes(n, 4, 0, 0, 32, 8), dtype=torch.uint8, device="cuda")
+    ms = timed(lambda: rs.radix_sort_keys(k32, ko, 0, 32, 8, temp=temp))
+    o = _order_key(torch, ko, "u32")
+    ok = not bool((o[1:] < o[:-1]).any()) and torch.equal(
+        torch.sort(_order_key(torch, k32, "u32")).values, o)
+    out["u32_keys"] = entry(ms, n, n * (4 + 4 * 8), ok, digit_bits=8, passes=4)
+    del ko, temp
+
+    # typed 32-bit key-value sorts on the same bit patterns (f32 includes
+    # every special pattern the uniform words produce: NaNs, infinities, -0)
+    vals = torch.from_numpy(workloads.index_payload(n).view(np.int32)).cuda()
+    ko, vo = torch.empty_like(k32), torch.empty_like(vals)
+    temp = torch.empty(rs.temp_bytes(n, 4, 4, 0, 32, 8), dtype=torch.uint8, device="cuda")
+    for kt, desc in (("f32", False), ("f32", True), ("i32", False)):
+        kin = k32.view(torch.float32) if kt == "f32" else k32
+        kout = ko.view(torch.float32) if kt == "f32" else ko
+        ms = timed(lambda: rs.radix_sort_pairs(kin, vals, kout, vo, temp=temp, key_type=kt,
+                                               descending=desc))
+        ok = _check_sorted_pairs(torch, k32, ko, vo, None, _order_key(torch, ko, kt, desc))
+        out[f"{kt}_pairs{'_desc' if desc else ''}"] = entry(ms, n, n * (4 + 4 * 16), ok)
+    del k32, ko, vo, temp
+
+    # u64 keys + u32 payload: histogram read 8 B + P passes x (read + write) 12 B
+    for name, gen, end in (("u64_pairs_uniform", workloads.u64_uniform, 64),
+                           ("u64_pairs_skewed", workloads.u64_skewed, 64),
+                           ("u64_pairs_bits0_39", workloads.u64_uniform, 40)):
+        k64 = torch.from_numpy(gen(n, 0).view(np.int64)).cuda()
+        ko, vo = torch.empty_like(k64), torch.empty_like(vals)
+        temp = torch.empty(rs.temp_bytes(n, 8, 4, 0, end, 8), dtype=torch.uint8, device="cuda")
+        ms = timed(lambda: rs.radix_sort_pairs(k64, vals, ko, vo, 0, end, 8, temp=temp))
+        masked = ko if end == 64 else ko & ((1 << end) - 1)
+        ok = _check_sorted_pairs(torch, k64, ko, vo, None,
+                                 _order_key(torch, masked, "u64" if end == 64 else "i64"))
+        passes = (end + 7) // 8
+        out[name] = entry(ms, n, n * (8 + passes * 24), ok, passes=passes)
+        del k64, ko, vo, temp
+    del vals
+
+    # row-wise 16-bit float sorts, (1024, 65536), int64 indices; minimum bytes:
+    # histogram read 2 B, pass 0 read 2 / write 2 + 4 (int32 index), pass 1
+    # read 2 + 4 / write 2 + 8 (int64 index)
+    rows, cols = 1024, 65536
+    for kind in ("f16", "bf16"):
+        x = torch.from_numpy(workloads.rows16(rows, cols, kind, 0).view(np.int16)).cuda()
+        x = x.view(torch.float16 if kind == "f16" else torch.bfloat16)
+        v = torch.empty_like(x)
+        i = torch.empty((rows, cols), dtype=torch.int64, device="cuda")
+        temp = torch.empty(rs.segmented_temp_bytes(rows, cols), dtype=torch.uint8, device="cuda")
+        for desc in (False, True):
+            ms = timed(lambda: rs.segmented_sort(x, desc, values_out=v, indices_out=i, temp=temp))
+            xi = x.view(torch.int16)
+            gathered = torch.equal(torch.gather(xi, 1, i), v.view(torch.int16))
+            u = xi.to(torch.int64) & 0xFFFF
+            t = torch.where(u >= 0x8000, u ^ 0xFFFF, u | 0x8000)
+            t = (0xFFFF - t) if desc else t
+            tv = torch.gather(t, 1, i)
+            ok = gathered and not bool((tv[:, 1:] < tv[:, :-1]).any()) and not bool(
+                ((tv[:, 1:] == tv[:, :-1]) & (i[:, 1:] < i[:, :-1])).any())
+            out[f"rows_{kind}_{rows}x{cols}{'_desc' if desc else ''}"] = entry(
+                ms, rows * cols, rows * cols * 26, ok)
+        del x, v, i, temp
+    return out
+
+
 ROW_SHAPES = [(64, 64), (256, 256), (1024, 1024), (4096, 4096), (1024, 65536), (1024, 1),
               (1024, 512), (16, 131072), (8, 262144)]
 
@@ -396,6 +525,7 @@ def main():
     ap.add_argument("--no-copy-probe", action="store_true")
     ap.add_argument("--no-small-sorts", action="store_true")
     ap.add_argument("--no-rows", action="store_true")
+    ap.add_argument("--no-configs", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -640,6 +770,9 @@ def main():
                                                 "passes_run": rs.passes_run(temp)}
                 rs.set_pass_skipping(False)
 
+    cfg_tab = None
+    if not args.no_configs and args.n_log2 == 28:
+        cfg_tab = config_sorts(rs, torch, workloads, args.n_log2, peak)
     small = None
     keys_cfg = None
     if not args.no_small_sorts:
@@ -673,7 +806,8 @@ def main():
                         "frac_of_peak": total_ideal / (ms_max * 1e-3) / 1e9 / peak},
                 "e2e": e2e, "gpu_launches": launches, "kernels": kernels,
                 "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks,
-                "distributions": dists, "small_sorts": small, "keys_only_configs": keys_cfg,
+                "distributions": dists, "configs": cfg_tab, "small_sorts": small,
+                "keys_only_configs": keys_cfg,
                 "row_sorts": rows_tab}
         print(json.dumps(line), flush=True)
     if world > 1:
