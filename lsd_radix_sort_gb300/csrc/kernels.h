@@ -173,7 +173,6 @@ struct SweepArgs {
   int64_t rows, cols;
   int64_t tiles_per_row;
   int64_t full_per_row;    // tiles of a row that hold a whole tile of keys
-  int full_tile;           // keys per full tile (set by the pass launcher)
   int shift;
   uint32_t mask;
   KeyXform xf;             // key transform

@@ -39,12 +39,13 @@
 //     every digit's keys leave as one contiguous run ("100 Days of GPU",
 //     day 35: after the local sort the write out is one run per digit).
 //     Payloads follow through the same staging buffer.
-// The last, partial tile of each row runs in a separate tail kernel after
-// the full tiles (nothing in the row waits on it), so the full-tile kernel
-// has no bounds checks.  In the tail, lanes past the end of the row take the
-// highest digit, rank after every real key of the tile, are not counted in
-// the published counts and are not stored (the page's sentinel padding,
-// without the padding).
+// The last, partial tile of each row takes a tile id after every full tile
+// of the pass (nothing waits on it; it waits only on full tiles of its row,
+// which have smaller ids), so it runs in the same launch on a separate code
+// path: the full-tile path has no bounds checks.  In a partial tile, lanes
+// past the end of the row take the highest digit, rank after every real key
+// of the tile, are not counted in the published counts and are not stored
+// (the page's sentinel padding, without the padding).
 #pragma once
 #include "common.cuh"
 #include "kernels.h"
@@ -468,16 +469,13 @@ struct SweepSmem {
   uint32_t abort;
 };
 
-// One CTA, one tile.  TAIL = false: the full tiles of every row, taken in
-// row-major order from the tile counter.  TAIL = true: the last, partial
-// tile of each row (CTA r takes row r's).  Within a row no tile waits on the
-// partial one, so the tail kernel runs after the full tiles are done; keeping
-// it out of the full-tile kernel leaves that kernel's registers to full tiles.
+// One CTA, one tile, taken from the tile counter: ids below
+// rows * full_per_row are the full tiles of every row, in row-major order;
+// id rows * full_per_row + r is row r's partial last tile, if rows have one.
 // DYN: the schedule (which passes run, between which buffers) comes from
 // K-SCAN through the tile counter; otherwise it is the host's static one in
 // the kernel arguments (every pass runs).
-template <bool TAIL, bool DYN, bool PRE, class KeyOp, int BITS, int VK, int THREADS, int ITEMS,
-          int WIN>
+template <bool DYN, bool PRE, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
 __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
   using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
   using T = typename KeyOp::T;
@@ -493,7 +491,7 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
 
   // the tile id and this pass's schedule code in one word
   if (tid == 0) {
-    const uint32_t v = TAIL ? ld_relaxed(a.tile_counter) : atomicAdd(a.tile_counter, 1u);
+    const uint32_t v = atomicAdd(a.tile_counter, 1u);
     s.tile_id = v & kTileMask;
     if (DYN) s.scratch.code = v >> kCodeShift;
     s.abort = ld_relaxed(a.error) != kErrNone;
@@ -503,21 +501,23 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
     reinterpret_cast<uint4*>(&s.scratch.warp_cnt[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
 
+  const uint32_t fpr = static_cast<uint32_t>(a.full_per_row);
+  const uint32_t n_full = static_cast<uint32_t>(a.rows) * fpr;
+  const bool full = s.tile_id < n_full;
   int64_t row, t, tile_begin;
-  if (TAIL) {
-    row = blockIdx.x;
+  if (!full) {
+    row = s.tile_id - n_full;
     t = a.full_per_row;
-    tile_begin = t * a.full_tile;
+    tile_begin = t * TILE;
   } else {
     // tile ids and tiles per row fit 32 bits (at most 2^30 keys)
     const uint32_t id = s.tile_id;
-    const uint32_t fpr = static_cast<uint32_t>(a.full_per_row);
     const uint32_t r32 = id / fpr;
     row = r32;
     t = id - r32 * fpr;
     tile_begin = t * TILE;
   }
-  const int valid = TAIL ? static_cast<int>(a.cols - tile_begin) : TILE;
+  const int valid = full ? TILE : static_cast<int>(a.cols - tile_begin);
   const int64_t off = row * a.cols + tile_begin;
   if (DYN && (s.scratch.code & kCodeSkip)) return;  // an identity pass: not run
   const PassBufs<DYN> pb{DYN ? s.scratch.code : a.code, a};
@@ -531,7 +531,7 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
   io.val_bar = nullptr;
   io.vals_in = false;
   if (s.abort) {  // an earlier tile failed: release successors and stop
-    if (!TAIL && !PRE && tid < R) st_relaxed(status_row + t * R + tid, kFlagP);
+    if (full && !PRE && tid < R) st_relaxed(status_row + t * R + tid, kFlagP);
   } else {
     if (VK != kValNone && pb.template vals_in<VK>() != nullptr) {
       // Payloads are not needed before the staging step: a full tile with an
@@ -541,7 +541,7 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
       // barrier makes them visible.
       const uint32_t* vsrc = static_cast<const uint32_t*>(pb.template vals_in<VK>()) + off;
       io.vals_in = true;
-      if (LSDRS_VALS_TMA && !TAIL && (reinterpret_cast<uintptr_t>(vsrc) & 15) == 0) {
+      if (LSDRS_VALS_TMA && full && (reinterpret_cast<uintptr_t>(vsrc) & 15) == 0) {
         if (tid == 0) {
           mbar_init(&s.bar, 1);
           mbar_arrive_expect_tx(&s.bar, TILE * sizeof(uint32_t));
@@ -552,24 +552,25 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
         for (int i = tid; i < valid; i += THREADS) s.vals[i] = ld_stream(vsrc + i);
       }
     }
-    sweep_tile<!TAIL, DYN, PRE, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io, status_row,
-                                                                   row, t,
-                                                           tile_begin, valid);
+    if (!full) {
+      sweep_tile<false, DYN, PRE, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io,
+                                                                       status_row, row, t,
+                                                                       tile_begin, valid);
+    } else {
+      sweep_tile<true, DYN, PRE, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io,
+                                                                      status_row, row, t,
+                                                                      tile_begin, valid);
+    }
   }
   uint32_t* zero = PassBufs<DYN>{DYN ? s.scratch.code : a.code, a}.status_zero();
-  if (!TAIL && !PRE && zero != nullptr && tid < R)
+  if (full && !PRE && zero != nullptr && tid < R)
     zero[static_cast<int64_t>(s.tile_id) * R + tid] = 0;
 }
 
 template <bool DYN, bool PRE, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB,
           int WIN>
 __global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
-  onesweep_body<false, DYN, PRE, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a);
-}
-
-template <bool DYN, bool PRE, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
-__global__ void __launch_bounds__(THREADS, 1) onesweep_tail_kernel(SweepArgs a) {
-  onesweep_body<true, DYN, PRE, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a);
+  onesweep_body<DYN, PRE, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a);
 }
 
 template <class K>
@@ -584,45 +585,26 @@ cudaError_t launch_with_smem(K kern, unsigned grid, int threads, size_t smem, cu
   return cudaGetLastError();
 }
 
-// The tail kernel runs one CTA per row, alone on the GPU: it takes a wide
-// CTA with few keys per thread, so that one partial tile is ranked by
-// 32 warps instead of 8.
-constexpr int kTailThreads = 1024;
-
-// One pass: the full tiles, then the partial tile of each row.  Returns
-// the number of kernels launched in *launched.
+// One pass: every full tile, then each row's partial tile, in one launch.
+// Returns the number of kernels launched in *launched.
 // PRE: offsets precomputed by the tile-count kernels (row-wise sorts only).
 template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB, int WIN,
           bool PRE = false>
 cudaError_t launch_sweep_t(const SweepArgs& args, int* launched, cudaStream_t s) {
   using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
   constexpr int TILE = S::kTile;
-  constexpr int TAIL_ITEMS = (TILE + kTailThreads - 1) / kTailThreads;
-  using ST = SweepSmem<KeyOp, BITS, VK, kTailThreads, TAIL_ITEMS>;
-  static_assert(ST::kTile >= TILE, "a tail tile holds any partial tile");
   SweepArgs a = args;
-  a.full_tile = TILE;
   *launched = 0;
   const int64_t full = a.rows * a.full_per_row;
-  if (full > 0) {
+  const bool partial = a.rows > 0 && a.cols % TILE != 0;
+  const int64_t grid = full + (partial ? a.rows : 0);
+  if (grid > 0) {
     cudaError_t e =
         a.dynamic
             ? launch_with_smem(onesweep_kernel<true, PRE, KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>,
-                               static_cast<unsigned>(full), THREADS, sizeof(S), s, a)
+                               static_cast<unsigned>(grid), THREADS, sizeof(S), s, a)
             : launch_with_smem(onesweep_kernel<false, PRE, KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>,
-                               static_cast<unsigned>(full), THREADS, sizeof(S), s, a);
-    if (e != cudaSuccess) return e;
-    ++*launched;
-  }
-  if (a.rows > 0 && a.cols % TILE != 0) {
-    cudaError_t e =
-        a.dynamic
-            ? launch_with_smem(onesweep_tail_kernel<true, PRE, KeyOp, BITS, VK, kTailThreads,
-                                                    TAIL_ITEMS, WIN>,
-                               static_cast<unsigned>(a.rows), kTailThreads, sizeof(ST), s, a)
-            : launch_with_smem(onesweep_tail_kernel<false, PRE, KeyOp, BITS, VK, kTailThreads,
-                                                    TAIL_ITEMS, WIN>,
-                               static_cast<unsigned>(a.rows), kTailThreads, sizeof(ST), s, a);
+                               static_cast<unsigned>(grid), THREADS, sizeof(S), s, a);
     if (e != cudaSuccess) return e;
     ++*launched;
   }
