@@ -88,3 +88,38 @@ def test_max_over_ranks_gloo(world):
         assert p.exitcode == 0
     got = sorted(q.get(timeout=10) for _ in range(world))
     assert [v for _, v in got] == [1.5 + world - 1] * world
+
+
+def test_result_checks_accept_the_oracle_and_reject_a_broken_tie():
+    """The device-side result checks bench.py applies to its larger workloads
+    (payload gather, order of the transformed key, ties in input order),
+    run on CPU tensors: the oracle's stable sort passes, the same result
+    with two tied payloads swapped fails, for every key type they cover."""
+    import numpy as np
+    import torch
+    import oracle
+    from lsd_radix_sort_gb300 import workloads
+    n = 5000
+    k = workloads.u32_uniform(n, 3)
+    k[::7] = k[1]
+    v = workloads.index_payload(n)
+    for kt, desc in (("u32", False), ("f32", False), ("f32", True), ("i32", False)):
+        arr = k.view(np.float32) if kt == "f32" else (k.view(np.int32) if kt == "i32" else k)
+        ek, ev = oracle.sort_typed(arr, kt, v, desc)
+        kin = torch.from_numpy(k.view(np.int32))
+        ko = torch.from_numpy(np.ascontiguousarray(ek).view(np.int32))
+        vo = torch.from_numpy(ev.view(np.int32))
+        order = bench._order_key(torch, ko, kt, desc)
+        assert bench._check_sorted_pairs(torch, kin, ko, vo, None, order)
+        j = int(torch.nonzero(order[1:] == order[:-1])[0])
+        bad = vo.clone()
+        bad[j], bad[j + 1] = vo[j + 1].item(), vo[j].item()
+        assert not bench._check_sorted_pairs(torch, kin, ko, bad, None, order)
+    k64 = workloads.u64_skewed(n, 0)
+    for end in (64, 40):
+        ek, ev = oracle.sort(k64, v, 0, end, 8)
+        ko = torch.from_numpy(ek.view(np.int64))
+        key = ko if end == 64 else ko & ((1 << end) - 1)
+        order = bench._order_key(torch, key, "u64" if end == 64 else "i64")
+        assert bench._check_sorted_pairs(torch, torch.from_numpy(k64.view(np.int64)), ko,
+                                         torch.from_numpy(ev.view(np.int32)), None, order)
