@@ -155,6 +155,16 @@ def _key_bytes(t) -> int:
     return es
 
 
+def _require_like(out, numel: int, elem: int, what: str):
+    """A caller-supplied output must hold exactly the elements the sort
+    writes, of the element width it writes; checked before any launch."""
+    if out is None:
+        return
+    if out.numel() != numel or out.element_size() != elem:
+        raise ValueError(f"{what} must hold {numel} elements of {elem} bytes, "
+                         f"got {out.numel()} of {out.element_size()}")
+
+
 def _require_cuda(*ts):
     for t in ts:
         if t is None:
@@ -186,6 +196,7 @@ def _temp(nbytes: int, device, temp=None):
     if temp is not None:
         if temp.numel() * temp.element_size() < nbytes:
             raise RadixSortError(RS_ERR_TEMP_TOO_SMALL, "scratch buffer")
+        _require_cuda(temp)
         return temp
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
 
@@ -211,8 +222,9 @@ def radix_sort_keys(keys, out=None, begin_bit: int = 0, end_bit: int | None = No
     import torch
     lib = load_library()
     keys = keys.reshape(-1)
-    _require_cuda(keys)
     kb = _key_bytes(keys)
+    _require_like(out, keys.numel(), kb, "out")
+    _require_cuda(keys)
     end_bit = kb * 8 if end_bit is None else end_bit
     if out is None:
         out = torch.empty_like(keys)
@@ -242,10 +254,12 @@ def radix_sort_pairs(keys, values, keys_out=None, values_out=None, begin_bit: in
     lib = load_library()
     keys = keys.reshape(-1)
     values = values.reshape(-1)
-    _require_cuda(keys, values)
     kb = _key_bytes(keys)
     if values.element_size() != 4 or values.numel() != keys.numel():
         raise ValueError("values must be 4-byte and one per key")
+    _require_like(keys_out, keys.numel(), kb, "keys_out")
+    _require_like(values_out, keys.numel(), 4, "values_out")
+    _require_cuda(keys, values)
     end_bit = kb * 8 if end_bit is None else end_bit
     keys_out = torch.empty_like(keys) if keys_out is None else keys_out
     values_out = torch.empty_like(values) if values_out is None else values_out
@@ -281,8 +295,14 @@ def segmented_sort(x, descending: bool = False, values_out=None, indices_out=Non
         raise TypeError("segmented_sort expects float16 or bfloat16 rows")
     if x.dim() != 2:
         raise ValueError("segmented_sort expects a 2-D tensor")
-    _require_cuda(x)
     rows, cols = x.shape
+    if values_out is not None and tuple(values_out.shape) != (rows, cols):
+        raise ValueError(f"values_out must have shape {(rows, cols)}")
+    _require_like(values_out, rows * cols, 2, "values_out")
+    if indices_out is not None and (tuple(indices_out.shape) != (rows, cols)
+                                    or indices_out.dtype != torch.int64):
+        raise ValueError(f"indices_out must be int64 of shape {(rows, cols)}")
+    _require_cuda(x)
     kind = RS_BF16 if x.dtype == torch.bfloat16 else RS_F16
     vals = torch.empty_like(x) if values_out is None else values_out
     idx = torch.empty((rows, cols), dtype=torch.int64, device=x.device) \
@@ -352,7 +372,11 @@ def device_status(temp, stream=None) -> int:
 
 
 def copy_probe(dst, src, stream=None):
+    """Streaming copy of ``src`` into ``dst`` (the bandwidth probe)."""
     nbytes = src.numel() * src.element_size()
+    if dst.numel() * dst.element_size() < nbytes:
+        raise ValueError("dst is smaller than src")
+    _require_cuda(dst, src)
     _check(load_library().rs_copy_probe(_ptr(dst), _ptr(src), nbytes, _stream_ptr(stream)),
            "rs_copy_probe")
 
