@@ -90,6 +90,9 @@ rs_status make_plan(KeyKind key, ValKind val, int64_t rows, int64_t cols, int be
   p.key_bytes = (key == kKeyU32 || key == kKeyX32) ? 4 : (key == kKeyU64 || key == kKeyX64) ? 8 : 2;
   const int kbits = p.key_bytes * 8;
   if (rows < 0 || cols < 0 || static_cast<uint64_t>(cols) > RS_MAX_KEYS) return RS_ERR_INVALID;
+  // every row is at least one tile, and tile ids are 24 bits (this also keeps
+  // rows * tiles_per_row and rows * cols far from overflowing)
+  if (rows > static_cast<int64_t>(kTileMask)) return RS_ERR_INVALID;
   if (begin_bit < 0 || end_bit > kbits || begin_bit >= end_bit) return RS_ERR_INVALID;
   if (bits < 1 || bits > 8) return RS_ERR_INVALID;
   p.rows = rows;

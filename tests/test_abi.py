@@ -53,6 +53,7 @@ def test_temp_bytes_query(lib):
     assert lib.radix_sort_temp_bytes(1 << 20, 4, 0, 0, 32, 8, ctypes.byref(small)) == 0
     assert small.value < out.value
     assert lib.radix_segmented_sort_temp_bytes(1024, 65536, ctypes.byref(out)) == 0
+    assert lib.radix_segmented_sort_temp_bytes(1 << 40, 1 << 10, ctypes.byref(out)) == 1
     assert out.value >= 1024 * 65536 * 6  # alternate keys + int32 indices
     assert lib.radix_sort_temp_bytes(0, 4, 0, 0, 32, 8, ctypes.byref(out)) == 0
 
@@ -103,6 +104,11 @@ def test_sort_calls_validate_before_launch(lib):
     assert lib.radix_segmented_sort_f16(bogus, bogus, bogus, 2, 2, 0, 2, temp, big, None) == 1
     assert lib.radix_segmented_sort_f16(bogus, bogus, bogus, -1, 2, 0, 0, temp, big, None) == 1
     assert lib.radix_segmented_sort_f16(bogus, bogus, bogus, 0, 5, 0, 0, temp, big, None) == 0
+    # more rows than tile ids (and rows * cols past any buffer): refused
+    assert lib.radix_segmented_sort_f16(bogus, bogus, bogus, 1 << 40, 1 << 20, 0, 0, temp, big,
+                                        None) == 1
+    assert lib.radix_segmented_sort_f16(bogus, bogus, bogus, 1 << 62, 4, 0, 0, temp, big,
+                                        None) == 1
     # typed sorts: unknown key type, bad descending flag, bad bit range, n == 0
     assert lib.radix_sort_keys_typed(9, 0, bogus, bogus, 100, 0, 32, 8, temp, big, None) == 1
     assert lib.radix_sort_keys_typed(-1, 0, bogus, bogus, 100, 0, 32, 8, temp, big, None) == 1
