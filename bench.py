@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -69,11 +70,27 @@ def load_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def onesweep_source_hash() -> str:
+SWEEP_SOURCES = ("onesweep.cuh", "sweep_u32.cu", "kernels.h", "common.cuh", "keys.cuh")
+
+
+def code_only(text: str) -> str:
+    """C++ source without comments and with whitespace collapsed, so that a
+    change of wording in a comment does not count as a change of the kernel."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def onesweep_source_hash(read=None) -> str:
+    """Hash of the code (comments stripped) the u32 scatter kernel is built
+    from; `read(name)` returns a file's text (default: the working tree)."""
+    if read is None:
+        def read(name):
+            with open(os.path.join(ROOT, "lsd_radix_sort_gb300", "csrc", name)) as fh:
+                return fh.read()
     h = hashlib.sha256()
-    for f in ("onesweep.cuh", "sweep_u32.cu", "kernels.h", "common.cuh", "keys.cuh"):
-        with open(os.path.join(ROOT, "lsd_radix_sort_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    for f in SWEEP_SOURCES:
+        h.update(code_only(read(f)).encode())
     return h.hexdigest()[:16]
 
 

@@ -179,7 +179,9 @@ struct SweepArgs {
   const uint32_t* bases;   // bases of this pass for row 0
   int64_t bases_row_stride;
   uint32_t* status_arr[2]; // look-back words [rows * full_per_row][radix], by parity
-  uint32_t* tile_counter;  // (schedule code << kCodeShift, when dynamic) | tiles handed out
+  uint32_t* tile_counter;  // (schedule code << kCodeShift, when dynamic) | tiles handed out:
+                           // ids below rows * full_per_row are full tiles, then one
+                           // partial tile per row when cols is not a whole number of tiles
   int dynamic;             // the schedule comes from K-SCAN (pass skipping on)
   uint32_t code;           // otherwise: this pass's code, from the host, and
   const void* pass_keys_in;   // the buffers and look-back words it selects
@@ -196,8 +198,9 @@ struct SweepArgs {
 cudaError_t launch_hist(KeyKind k, int bits, const HistArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_hist_x(KeyKind k, int bits, const HistArgs& a, int grid, cudaStream_t s);
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
-// One scatter pass: a kernel over the full tiles, then one over each row's
-// partial tile; *launched receives the number of kernels launched (0-2).
+// One scatter pass: one kernel over every full tile and then each row's
+// partial tile (tile ids in that order); *launched receives the number of
+// kernels launched (0 or 1).
 cudaError_t launch_sweep_u32(ValKind v, int bits, const SweepArgs& a, int* launched,
                              cudaStream_t s);
 cudaError_t launch_sweep_u64(ValKind v, int bits, const SweepArgs& a, int* launched,

@@ -123,3 +123,17 @@ def test_result_checks_accept_the_oracle_and_reject_a_broken_tie():
         order = bench._order_key(torch, key, "u64" if end == 64 else "i64")
         assert bench._check_sorted_pairs(torch, torch.from_numpy(k64.view(np.int64)), ko,
                                          torch.from_numpy(ev.view(np.int32)), None, order)
+
+
+def test_kernel_hash_ignores_comments_only():
+    """The traffic record stays valid across comment edits of the kernel
+    sources and is dropped when the code changes."""
+    src = "int f(int x) {  // twice\n  /* the\n value */ return 2 * x;\n}\n"
+    assert bench.code_only(src) == bench.code_only(src.replace("twice", "two times"))
+    assert bench.code_only(src) != bench.code_only(src.replace("2 * x", "3 * x"))
+    files = {name: src for name in bench.SWEEP_SOURCES}
+    h = bench.onesweep_source_hash(lambda name: files[name])
+    files["kernels.h"] = src.replace("// twice", "// doubled")
+    assert bench.onesweep_source_hash(lambda name: files[name]) == h
+    files["kernels.h"] = src.replace("return", "return 1 +")
+    assert bench.onesweep_source_hash(lambda name: files[name]) != h
