@@ -7,7 +7,7 @@ import torch
 
 import oracle
 from lsd_radix_sort_gb300 import workloads
-from tests.gpu_util import field, poisoned_like, to_dev, to_host
+from tests.gpu_util import assert_pairs, field, poisoned_like, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -44,7 +44,7 @@ def test_1024_keys_below_4096_three_hex_passes(rs):
     assert np.array_equal(got, exp)
     kp, vp = run_pairs(rs, keys, workloads.index_payload(1024), 0, 12, 4)
     ek, ev = oracle.sort(keys, workloads.index_payload(1024), 0, 12, 4)
-    assert np.array_equal(kp, ek) and np.array_equal(vp, ev)
+    assert_pairs(kp, vp, ek, ev)
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2])
@@ -63,7 +63,7 @@ def test_page_size_not_a_tile_multiple(rs):
     for bits in (4, 8):
         ko, vo = run_pairs(rs, keys, vals, 0, 32, bits)
         ek, ev = oracle.sort(keys, vals, 0, 32, bits)
-        assert np.array_equal(ko, ek) and np.array_equal(vo, ev)
+        assert_pairs(ko, vo, ek, ev)
 
 
 @pytest.mark.parametrize("dist", list(workloads.U32_DISTRIBUTIONS))
@@ -85,7 +85,7 @@ def test_u64_pairs_and_keys(rs, dist, begin, end):
     vals = workloads.index_payload(n)
     ko, vo = run_pairs(rs, keys, vals, begin, end, 8)
     ek, ev = oracle.sort(keys, vals, begin, end, 8)
-    assert np.array_equal(ko, ek) and np.array_equal(vo, ev)
+    assert_pairs(ko, vo, ek, ev)
     k2 = run_keys(rs, keys, begin, end, 8)
     assert np.array_equal(k2, ek)
 
@@ -116,13 +116,13 @@ def test_ragged_sizes(rs, n, short_rows_one_kernel):
     for bits in (8, 5):
         ko, vo = run_pairs(rs, keys, vals, 0, 32, bits)
         ek, ev = oracle.sort(keys, vals, 0, 32, bits)
-        assert np.array_equal(ko, ek) and np.array_equal(vo, ev), bits
+        assert_pairs(ko, vo, ek, ev, f"b={bits}")
         assert np.array_equal(run_keys(rs, keys, 0, 32, bits), ek)
     k64 = workloads.u64_uniform(n, 12)
     assert np.array_equal(run_keys(rs, k64, 0, 64, 8), oracle.sort(k64, None, 0, 64, 8)[0])
     k64o, v64o = run_pairs(rs, k64, vals, 0, 64, 8)
     e64, ev64 = oracle.sort(k64, vals, 0, 64, 8)
-    assert np.array_equal(k64o, e64) and np.array_equal(v64o, ev64)
+    assert_pairs(k64o, v64o, e64, ev64)
 
 
 @pytest.mark.parametrize("bits", [1, 2, 3, 4, 5, 6, 7, 8])
@@ -132,11 +132,11 @@ def test_every_digit_width(rs, bits):
     vals = workloads.index_payload(n)
     ko, vo = run_pairs(rs, keys, vals, 0, 24, bits)
     ek, ev = oracle.sort(keys, vals, 0, 24, bits)
-    assert np.array_equal(ko, ek) and np.array_equal(vo, ev)
+    assert_pairs(ko, vo, ek, ev)
     k64 = workloads.u64_uniform(n, 22)
     k64o, v64o = run_pairs(rs, k64, vals, 5, 37, bits)
     e64, ev64 = oracle.sort(k64, vals, 5, 37, bits)
-    assert np.array_equal(k64o, e64) and np.array_equal(v64o, ev64)
+    assert_pairs(k64o, v64o, e64, ev64)
 
 
 @pytest.mark.parametrize("begin,end,bits", [(0, 1, 1), (31, 32, 8), (3, 29, 7), (8, 24, 3),
@@ -185,7 +185,7 @@ def test_max_digit_runs_cross_many_tiles(rs):
     vals = workloads.index_payload(n)
     ko, vo = run_pairs(rs, keys, vals)
     ek, ev = oracle.sort(keys, vals)
-    assert np.array_equal(ko, ek) and np.array_equal(vo, ev)
+    assert_pairs(ko, vo, ek, ev)
 
 
 # -------------------------------------------------------------- histograms

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from lsd_radix_sort_gb300 import workloads
-from tests.gpu_util import poisoned_like, to_dev, to_host
+from tests.gpu_util import assert_pairs, poisoned_like, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -69,7 +69,7 @@ def test_skipped_passes_pairs(rs, case, in_place, n):
     vals = workloads.index_payload(n)
     ek, ev = oracle.sort(keys, vals, begin, end, bits)
     ko, vo, run = sort_pairs(rs, keys, vals, begin, end, bits, in_place)
-    assert np.array_equal(ko, ek) and np.array_equal(vo, ev)
+    assert_pairs(ko, vo, ek, ev)
     # short inputs are sorted by one kernel in shared memory, every pass
     # included
     assert run == (want_run if n > rs.SMALL_SORT_MAX_KEYS else oracle.num_passes(begin, end, bits))
@@ -94,7 +94,8 @@ def test_skipping_off_runs_every_pass(rs):
     ek, ev = oracle.sort(keys, vals, begin, end, bits)
     for in_place in (False, True):
         ko, vo, run = sort_pairs(rs, keys, vals, begin, end, bits, in_place)
-        assert np.array_equal(ko, ek) and np.array_equal(vo, ev) and run == 4
+        assert_pairs(ko, vo, ek, ev)
+        assert run == 4
 
 
 def test_no_pass_skipped_on_uniform_keys(rs):
@@ -102,7 +103,8 @@ def test_no_pass_skipped_on_uniform_keys(rs):
     vals = workloads.index_payload(100_000)
     ko, vo, run = sort_pairs(rs, keys, vals, 0, 32, 8, False)
     ek, ev = oracle.sort(keys, vals, 0, 32, 8)
-    assert np.array_equal(ko, ek) and np.array_equal(vo, ev) and run == 4
+    assert_pairs(ko, vo, ek, ev)
+    assert run == 4
 
 
 @pytest.mark.parametrize("in_place", [False, True])
