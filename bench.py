@@ -86,7 +86,8 @@ def onesweep_source_hash(read=None) -> str:
     from; `read(name)` returns a file's text (default: the working tree)."""
     if read is None:
         def read(name):
-            with open(os.path.join(ROOT, "lsd_radix_sort_gb300", "csrc", name)) as fh:
+            with open(os.path.join(ROOT, "lsd_radix_sort_gb300", "csrc", name), encoding="utf-8",
+                      errors="replace") as fh:
                 return fh.read()
     h = hashlib.sha256()
     for f in SWEEP_SOURCES:
