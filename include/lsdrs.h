@@ -14,6 +14,9 @@
  * into bases; then one "onesweep" scatter kernel per pass, in which tiles
  * rank their keys in shared memory, learn the counts of earlier tiles by a
  * decoupled look-back, and write each digit's keys as one contiguous run.
+ * A sort whose rows (the whole input, for a flat sort) hold at most 8,192
+ * keys, with 4- or 8-bit digits, runs in one kernel instead: one CTA per row
+ * does every pass in shared memory (see rs_set_small_sort).
  *
  * Conventions shared by every call:
  *  - Pointers marked (device) are device memory of the current device; the
