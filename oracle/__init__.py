@@ -65,7 +65,7 @@ def _load():
         lib.or_exclusive_scan.argtypes = [P, u32, P]
         lib.or_exclusive_scan.restype = None
         lib.or_stable_destinations.argtypes = [P, sz, u32, P, P]
-        lib.or_stable_destinations.restype = None
+        lib.or_stable_destinations.restype = i
         lib.or_counting_pass.argtypes = [P, sz, u32, P, P, P]
         lib.or_counting_pass.restype = i
         lib.or_num_passes.argtypes = [i, i, i]

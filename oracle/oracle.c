@@ -72,11 +72,12 @@ void or_exclusive_scan(const uint64_t *counts, uint32_t radix,
 
 /* 3. Stable destinations: walk the input in order; element i goes to its
  *    digit's running offset, which then advances (Listing 16-8 step 3;
- *    section 13.2 "pos[d]++" walk). */
-void or_stable_destinations(const uint32_t *digit, size_t n, uint32_t radix,
-                            const uint64_t *offsets, uint64_t *dest) {
+ *    section 13.2 "pos[d]++" walk).  Returns OR_ERR_NOMEM, with dest left
+ *    unwritten, when its working array cannot be allocated. */
+int or_stable_destinations(const uint32_t *digit, size_t n, uint32_t radix,
+                           const uint64_t *offsets, uint64_t *dest) {
   uint64_t *pos = (uint64_t *)malloc(sizeof(uint64_t) * radix);
-  if (!pos) return;
+  if (!pos) return OR_ERR_NOMEM;
   for (uint32_t d = 0; d < radix; d++) pos[d] = offsets[d];
   for (size_t i = 0; i < n; i++) {
     uint32_t d = digit[i];
@@ -84,6 +85,7 @@ void or_stable_destinations(const uint32_t *digit, size_t n, uint32_t radix,
     pos[d] += 1;
   }
   free(pos);
+  return OR_OK;
 }
 
 /* One whole pass on a digit array: dest[i] is where element i lands. */
@@ -94,8 +96,7 @@ int or_counting_pass(const uint32_t *digit, size_t n, uint32_t radix,
     if (digit[i] >= radix) return OR_ERR_INVALID;
   or_histogram(digit, n, radix, counts);
   or_exclusive_scan(counts, radix, offsets);
-  or_stable_destinations(digit, n, radix, offsets, dest);
-  return OR_OK;
+  return or_stable_destinations(digit, n, radix, offsets, dest);
 }
 
 /* ---- bit-field LSD sorts (Listing 16-9 driver with the readings above) ---- */
@@ -157,7 +158,8 @@ static int pass_width(int begin_bit, int end_bit, int b, int p) {
       KEY_T *dst = kbuf[1 - cur];                                              \
       for (size_t i = 0; i < n; i++)                                           \
         digit[i] = (uint32_t)((((uint64_t)src[i]) >> shift) & mask);           \
-      or_counting_pass(digit, n, radix, counts, offsets, dest);                \
+      rc = or_counting_pass(digit, n, radix, counts, offsets, dest);           \
+      if (rc != OR_OK) goto done;                                              \
       for (size_t i = 0; i < n; i++) dst[dest[i]] = src[i];                    \
       if (vals_in) {                                                           \
         const uint32_t *vs = vbuf[cur];                                        \
@@ -251,7 +253,8 @@ int or_segmented_sort16(const uint16_t *in, uint16_t *vals_out,
     for (int p = 0; p < 2; p++) {
       int shift = 8 * p;
       for (size_t i = 0; i < n; i++) digit[i] = (kb[cur][i] >> shift) & 0xFFu;
-      or_counting_pass(digit, n, radix, counts, offsets, dest);
+      rc = or_counting_pass(digit, n, radix, counts, offsets, dest);
+      if (rc != OR_OK) goto done;
       for (size_t i = 0; i < n; i++) {
         kb[1 - cur][dest[i]] = kb[cur][i];
         vb[1 - cur][dest[i]] = vb[cur][i];
