@@ -460,9 +460,8 @@ def row_sorts(rs, torch, workloads, reps: int = 20):
             return a.elapsed_time(b) / reps
         entry = {"torch_sort_ms": round(timed(lambda: torch.sort(x, dim=-1)), 4)}
         for mode, name in ((False, "lookback_ms"), (True, "precomputed_ms")):
-            rs.set_tile_offsets(mode)
-            entry[name] = round(timed(lambda: rs.segmented_sort(x, False, v, idx, temp)), 4)
-        rs.set_tile_offsets(False)
+            entry[name] = round(timed(lambda: rs.segmented_sort(x, False, v, idx, temp,
+                                                                tile_offsets=mode)), 4)
         out[f"{rows}x{cols}"] = entry
         del x, v, idx, temp
     return out
@@ -513,15 +512,15 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def time_sorts(rs, torch, dk, dv, ko, vo, temp, steps, warmup, stream):
+def time_sorts(rs, torch, dk, dv, ko, vo, temp, steps, warmup, stream, **opts):
     for _ in range(warmup):
-        rs.radix_sort_pairs(dk, dv, ko, vo, 0, 32, DIGIT_BITS, temp=temp)
+        rs.radix_sort_pairs(dk, dv, ko, vo, 0, 32, DIGIT_BITS, temp=temp, **opts)
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     stop = torch.cuda.Event(enable_timing=True)
     start.record(stream)
     for _ in range(steps):
-        rs.radix_sort_pairs(dk, dv, ko, vo, 0, 32, DIGIT_BITS, temp=temp)
+        rs.radix_sort_pairs(dk, dv, ko, vo, 0, 32, DIGIT_BITS, temp=temp, **opts)
     stop.record(stream)
     torch.cuda.synchronize()
     return start.elapsed_time(stop) / steps
@@ -781,12 +780,10 @@ def main():
             if name != "uniform":
                 # the same sort with pass skipping on: identity passes are not
                 # run, so the ideal-bytes model above does not apply
-                rs.set_pass_skipping(True)
                 sms = time_sorts(rs, torch, dk, dv, ko, vo, temp, max(args.steps // 2, 3), 3,
-                                 stream)
+                                 stream, pass_skipping=True)
                 dists[name]["pass_skipping"] = {"ms": sms, "gkeys_s": n / (sms * 1e-3) / 1e9,
                                                 "passes_run": rs.passes_run(temp)}
-                rs.set_pass_skipping(False)
 
     cfg_tab = None
     if not args.no_configs and args.n_log2 == 28:

@@ -16,7 +16,7 @@
  * decoupled look-back, and write each digit's keys as one contiguous run.
  * A sort whose rows (the whole input, for a flat sort) hold at most 8,192
  * keys, with 4- or 8-bit digits, runs in one kernel instead: one CTA per row
- * does every pass in shared memory (see rs_set_small_sort).
+ * does every pass in shared memory (see RS_OPT_NO_SMALL_SORT).
  *
  * Conventions shared by every call:
  *  - Pointers marked (device) are device memory of the current device; the
@@ -39,6 +39,10 @@
  *    returns RS_ERR_CUDA.  Errors raised on the device (a look-back wait
  *    that exceeded its time limit) are recorded in `temp` and returned by
  *    radix_sort_device_status().
+ *  - Modes (pass skipping, precomputed tile offsets, the one-kernel path for
+ *    short rows, the wait limit) are options of the call that wants them
+ *    (rs_options); the library keeps no mode state between calls, so calls
+ *    from different threads or streams never change each other's schedule.
  */
 #ifndef LSDRS_H
 #define LSDRS_H
@@ -66,20 +70,55 @@ typedef enum rs_key_type {
   RS_KEY_U64 = 3, RS_KEY_I64 = 4, RS_KEY_F64 = 5    /* 8-byte keys */
 } rs_key_type;
 
-/* Largest number of keys in one sort (or one row of a row-wise sort); the
- * device offsets are 32-bit and the bound matches the row limit of the
- * row-wise sort (FlagTree PR #1084: n < 2^30). */
-#define RS_MAX_KEYS ((size_t)((1u << 30) - 1u))
+/* Largest number of keys in one flat sort: output positions are 32-bit.
+ * The look-back words of a sort hold a flag pair and a count in 32 bits (a
+ * 30-bit count) below 2^30 keys, and in 64 bits (a 62-bit count) for a flat
+ * sort of 2^30 keys or more; the scratch size accounts for it. */
+#define RS_MAX_KEYS ((size_t)0xFFFFFFFFu)
+/* Largest row of a row-wise sort (FlagTree PR #1084, "radix_sort"
+ * signature: n < 2^30). */
+#define RS_MAX_ROW_KEYS ((size_t)((1u << 30) - 1u))
 
-/* Size in bytes of the scratch buffer a flat sort needs.
+/* Options of one sort call.  A NULL rs_options* means all defaults; a
+ * zero-initialised struct is the same.
+ *   flags  RS_OPT_* bits (unknown bits: RS_ERR_INVALID)
+ *     RS_OPT_PASS_SKIPPING  a pass in which every key (every key of every
+ *            row, for a row-wise sort) has the same digit is the identity
+ *            permutation and is not run; decided on the device from the
+ *            upfront histograms, so nothing waits, and the output is the
+ *            same.  Off by default: a sort of keys that vary in every digit
+ *            pays about 1% for the device-side schedule.
+ *     RS_OPT_TILE_OFFSETS   row-wise sorts only: before each pass a kernel
+ *            counts the digits of every tile and a per-row scan turns the
+ *            counts into offsets, so the scatter never waits on another tile
+ *            (FlagTree PR #1084, section 2, "precompute each tile"); it reads
+ *            the keys once more per pass.  Pass skipping does not apply.
+ *     RS_OPT_NO_SMALL_SORT  sorts whose rows hold at most 8,192 keys take the
+ *            multi-kernel path like longer rows instead of the one-kernel
+ *            path (which runs every pass: it never skips).
+ *   lookback_timeout_ns  limit on one look-back or copy wait inside the
+ *            scatter kernels; 0 = the default, 2 s; at most 60 s.  A wait
+ *            that runs past it records RS_ERR_LOOKBACK_TIMEOUT (read it with
+ *            radix_sort_device_status) and releases every later tile.
+ * The results never depend on the options. */
+typedef struct rs_options {
+  unsigned flags;
+  uint64_t lookback_timeout_ns;
+} rs_options;
+#define RS_OPT_PASS_SKIPPING 0x1u
+#define RS_OPT_TILE_OFFSETS 0x2u
+#define RS_OPT_NO_SMALL_SORT 0x4u
+
+/* Size in bytes of the scratch buffer a flat sort needs (keys only or
+ * key-value; the same size serves any options).
  *   n           number of keys (0 <= n <= RS_MAX_KEYS)
  *   key_bytes   4 (u32) or 8 (u64)
  *   value_bytes 0 (keys only) or 4 (u32 payload)
  *   begin_bit, end_bit, digit_bits  as for the sort calls
  * Writes the size to *bytes.  Host only; enqueues nothing. */
-rs_status radix_sort_temp_bytes(size_t n, int key_bytes, int value_bytes,
-                                int begin_bit, int end_bit, int digit_bits,
-                                size_t* bytes);
+rs_status radix_sort_keys_temp_bytes(size_t n, int key_bytes, int value_bytes,
+                                     int begin_bit, int end_bit, int digit_bits,
+                                     size_t* bytes);
 
 /* Keys-only LSD radix sort of n unsigned 32-bit keys.
  * (CUDA Handbook ch. 16, Listing 16-9 "RadixSort": one counting-sort pass per
@@ -89,8 +128,9 @@ rs_status radix_sort_temp_bytes(size_t n, int key_bytes, int value_bytes,
  *   n         0 <= n <= RS_MAX_KEYS; n == 0 enqueues nothing
  *   begin_bit 0 <= begin_bit < end_bit <= 32
  *   digit_bits 1..8 (2^digit_bits buckets per pass)
- *   temp, temp_bytes (device) scratch of at least radix_sort_temp_bytes()
- *   stream    cudaStream_t as void* */
+ *   temp, temp_bytes (device) scratch of at least radix_sort_keys_temp_bytes()
+ *   stream    cudaStream_t as void*
+ * Every option at its default (see radix_sort_keys_typed for options). */
 rs_status radix_sort_keys_u32(const uint32_t* keys_in, uint32_t* keys_out, size_t n,
                               int begin_bit, int end_bit, int digit_bits,
                               void* temp, size_t temp_bytes, void* stream);
@@ -131,19 +171,23 @@ rs_status radix_sort_pairs_u64(const uint64_t* keys_in, uint64_t* keys_out,
  *   type       an rs_key_type; 4-byte types take 4-byte keys, 8-byte 8-byte
  *   descending 0 or 1
  *   begin_bit, end_bit  the bits of T(k) sorted (all of them: 0 and 8*size)
- *   temp       scratch of radix_sort_temp_bytes() for the key size
+ *   temp       scratch of radix_sort_keys_temp_bytes() for the key size
+ *   opts       (host) options of this call, or NULL for the defaults
  * Other arguments and errors as radix_sort_keys_u32; an unknown type or a
- * descending flag other than 0/1 is RS_ERR_INVALID. */
+ * descending flag other than 0/1 is RS_ERR_INVALID.  RS_KEY_U32/RS_KEY_U64
+ * ascending is the unsigned sort with options. */
 rs_status radix_sort_keys_typed(rs_key_type type, int descending, const void* keys_in,
                                 void* keys_out, size_t n, int begin_bit, int end_bit,
-                                int digit_bits, void* temp, size_t temp_bytes, void* stream);
+                                int digit_bits, void* temp, size_t temp_bytes,
+                                const rs_options* opts, void* stream);
 
 /* Typed key-value sort: radix_sort_keys_typed with a u32 payload, as
  * radix_sort_pairs_u32. */
 rs_status radix_sort_pairs_typed(rs_key_type type, int descending, const void* keys_in,
                                  void* keys_out, const uint32_t* vals_in, uint32_t* vals_out,
                                  size_t n, int begin_bit, int end_bit, int digit_bits,
-                                 void* temp, size_t temp_bytes, void* stream);
+                                 void* temp, size_t temp_bytes, const rs_options* opts,
+                                 void* stream);
 
 /* Scratch size of a row-wise sort of a (rows, cols) 16-bit array. */
 rs_status radix_segmented_sort_temp_bytes(int64_t rows, int64_t cols, size_t* bytes);
@@ -157,18 +201,26 @@ rs_status radix_segmented_sort_temp_bytes(int64_t rows, int64_t cols, size_t* by
  *   vals_out  (device) rows*cols patterns: each row sorted
  *   idx_out   (device) rows*cols int64: idx_out[r][j] is the column of in[r]
  *             that landed at position j
- *   rows >= 0, 0 <= cols <= RS_MAX_KEYS; rows*cols == 0 enqueues nothing
+ *   rows >= 0, 0 <= cols <= RS_MAX_ROW_KEYS (cols <= RS_MAX_KEYS when
+ *             rows == 1); rows*cols == 0 enqueues nothing
  *   kind      RS_F16 or RS_BF16 (both orders come from the sign bit, so the
  *             result does not depend on it; it is validated and recorded)
  *   descending 0 = ascending, 1 = descending.  Ascending order is the order
  *             of the bijection T(u) = sign ? ~u : u | 0x8000: -NaN < -inf <
  *             negatives < -0 < +0 < positives < +inf < +NaN; descending is
  *             the order of ~T(u).  Equal patterns keep input order in both.
- *   temp, temp_bytes (device) scratch of radix_segmented_sort_temp_bytes() */
+ *   temp, temp_bytes (device) scratch of radix_segmented_sort_temp_bytes()
+ * Every option at its default. */
 rs_status radix_segmented_sort_f16(const uint16_t* in, uint16_t* vals_out, int64_t* idx_out,
                                    int64_t rows, int64_t cols, rs_float_kind kind,
                                    int descending, void* temp, size_t temp_bytes,
                                    void* stream);
+
+/* radix_segmented_sort_f16 with the options of this call (NULL: defaults). */
+rs_status radix_segmented_sort_f16_ex(const uint16_t* in, uint16_t* vals_out, int64_t* idx_out,
+                                      int64_t rows, int64_t cols, rs_float_kind kind,
+                                      int descending, void* temp, size_t temp_bytes,
+                                      const rs_options* opts, void* stream);
 
 /* Upfront all-pass digit histograms and their exclusive scans, the first two
  * stages of a sort, exposed on their own (FlagTree PR #1084, section 2:
@@ -178,7 +230,7 @@ rs_status radix_segmented_sort_f16(const uint16_t* in, uint16_t* vals_out, int64
  *   keys      (device) n keys of key_bytes (4 or 8) bytes
  *   hist_out  (device) passes * 2^digit_bits u32 counts, pass-major
  *   bases_out (device) the same shape: exclusive scan of each pass's counts
- *   temp      (device) scratch of radix_sort_temp_bytes(n, key_bytes, 0, ...) */
+ *   temp      (device) scratch of radix_sort_keys_temp_bytes(n, key_bytes, 0, ...) */
 rs_status radix_sort_histograms(const void* keys, int key_bytes, size_t n,
                                 int begin_bit, int end_bit, int digit_bits,
                                 uint32_t* hist_out, uint32_t* bases_out,
@@ -188,58 +240,19 @@ rs_status radix_sort_histograms(const void* keys, int key_bytes, size_t n,
  * that used `temp` (RS_OK or RS_ERR_LOOKBACK_TIMEOUT), or RS_ERR_CUDA. */
 rs_status radix_sort_device_status(const void* temp, void* stream);
 
-/* Pass skipping, for every sort enqueued after the call (process-wide;
- * default off).  With it on, a pass in which every key (every key of every
- * row, for a row-wise sort) has the same digit is the identity permutation
- * and is not run: the decision is taken on the device from the upfront
- * histograms, so nothing waits for it, and the output is the same.  A sort
- * of keys that vary in every digit pays about 1% for the device-side
- * schedule, which is why it is off by default.
- *   on   0 or 1 (anything else: RS_ERR_INVALID) */
-rs_status rs_set_pass_skipping(int on);
-
-/* How the row-wise sort finds each tile's output offsets, for every
- * row-wise sort enqueued after the call (process-wide):
- *   0 (default) decoupled look-back inside the scatter pass;
- *   1           precomputed: before each pass, a kernel counts the digits of
- *               every tile and a per-row scan turns the counts into offsets,
- *               so the scatter never waits on another tile (FlagTree PR
- *               #1084, section 2, "precompute each tile"); it reads the keys
- *               once more per pass.  Pass skipping does not apply in this mode.
- * Anything else: RS_ERR_INVALID.  The results are identical. */
-rs_status rs_set_tile_offsets(int precomputed);
-
 /* Passes run by the last sort enqueued with this scratch buffer (all of
- * them unless pass skipping is on).  Synchronises `stream` and reads the
+ * them unless RS_OPT_PASS_SKIPPING was given).  Synchronises `stream` and reads the
  * count.
  *   temp    (device) the scratch buffer of that sort
  *   passes  (host) receives the count (0 .. passes of the bit range) */
 rs_status radix_sort_passes_run(const void* temp, int* passes, void* stream);
 
-/* The one-kernel path for short rows, for every sort enqueued after the call
- * (process-wide; default on).  With it on, a sort whose rows (the whole
- * input, for a flat sort) hold at most 8,192 keys, with 4- or 8-bit digits,
- * runs in one kernel: one CTA per row loads the row into shared memory,
- * does every pass there (rank, digit scan, scatter within the row, which is
- * a single tile: CUDA Handbook ch. 16, Listing 16-8, on one tile) and
- * writes the sorted row once.  Off: such sorts take the multi-kernel path
- * (K-HIST, K-SCAN, one scatter kernel per pass) like longer rows.  The
- * results are identical; the multi-kernel path then also runs every pass
- * that pass skipping does not remove, which the one-kernel path never skips.
- *   on   0 or 1 (anything else: RS_ERR_INVALID) */
-rs_status rs_set_small_sort(int on);
-
 /* Human-readable name of a status code (static storage). */
 const char* rs_status_string(rs_status status);
 
-/* Limit in nanoseconds on one look-back wait inside the scatter kernels
- * (default 2 s).  A wait that runs past it records RS_ERR_LOOKBACK_TIMEOUT
- * and releases every later tile.  Process-wide; host only. */
-rs_status rs_set_lookback_timeout_ns(uint64_t ns);
-
 /* Failure-detection check: runs the scatter kernels' bounded look-back wait
  * on a status word that nothing ever sets, with the given limit
- * (0 < timeout_ns <= 10 s).  Writes the status the wait produced
+ * (0 < timeout_ns <= 60 s).  Writes the status the wait produced
  * (RS_ERR_LOOKBACK_TIMEOUT when it expired) to *result after synchronising
  * `stream`.  word: (device) two u32 scratch words (the status word and an
  * error word), overwritten. */
@@ -269,22 +282,37 @@ int rs_profile_read(rs_kernel_time* out, int max);
  * count for measurement); resets the counter. */
 uint64_t rs_launch_count_reset(void);
 
-/* Key-value sort for callers that cannot allocate device memory (the pages
- * have no counterpart of this entry point).  Same result and arguments as
- * radix_sort_pairs_u32 without temp/temp_bytes: the scratch is a fixed 4 MiB
- * array inside the library's device code, which every GPU that loads the
- * library holds until the process exits.
+/* Key-value sort for callers that cannot allocate device memory where they
+ * sort (the pages have no counterpart of this entry point): callers whose
+ * device memory belongs to a pool they may not grow, or plugins and
+ * callbacks handed only the buffers they work on, with no allocator of their
+ * own.  Same result and arguments as radix_sort_pairs_u32 without
+ * temp/temp_bytes, with every option at its default: the scratch is a fixed
+ * 4 MiB array inside the library's device code, which every GPU that loads
+ * the library holds until the process exits.  No call allocates or frees
+ * anything.
  *   n         0 <= n <= 262,144 (2^18); larger n returns RS_ERR_INVALID
  *             before anything is enqueued
  * The first call on a device looks up that device's address of the array
- * (make it before any stream capture on that device).  Every call on a device
- * shares the one array: calls whose work overlaps on the GPU (for example on
- * two streams) race and give wrong results; calls on one stream are safe.
- * Each call clears what it needs cleared; nothing else is allocated or freed. */
+ * (make that first call, or a call of radix_sort_pairs_u32_noalloc_status,
+ * before any stream capture on the device).  The address is kept for the
+ * life of the process: a process that resets a device (cudaDeviceReset) must
+ * not call these two entry points on it afterwards.  Every call on a device
+ * shares the one array and it keeps the last call's contents; each call
+ * clears what must start at zero.  Calls whose work overlaps on the GPU (for
+ * example on two streams) race and give wrong results; calls on one stream
+ * are safe. */
 rs_status radix_sort_pairs_u32_noalloc(const uint32_t* keys_in, uint32_t* keys_out,
                                        const uint32_t* vals_in, uint32_t* vals_out, size_t n,
                                        int begin_bit, int end_bit, int digit_bits,
                                        void* stream);
+
+/* Synchronises `stream` and returns the device-side status of the last
+ * radix_sort_pairs_u32_noalloc enqueued on the current device (RS_OK or
+ * RS_ERR_LOOKBACK_TIMEOUT), or RS_ERR_CUDA: the radix_sort_device_status of
+ * that entry point, whose scratch the caller cannot name.  Allocates
+ * nothing. */
+rs_status radix_sort_pairs_u32_noalloc_status(void* stream);
 
 #ifdef __cplusplus
 }

@@ -10,7 +10,11 @@ fails to load, every call raises.
 Keys may be given as 4-byte or 8-byte tensors; by default their bits are
 sorted as unsigned integers, and ``key_type`` ("i32", "f32", "i64", "f64",
 "u32", "u64") with ``descending`` selects the typed sorts.  Payloads are
-4-byte tensors.
+4-byte tensors.  Modes (pass skipping, precomputed tile offsets, the
+one-kernel path for short rows, the look-back wait limit) are keyword
+arguments of each call: the library holds no
+mode state, so calls on different threads or streams never affect each
+other.
 """
 from __future__ import annotations
 
@@ -23,32 +27,34 @@ from . import build as _build
 __all__ = [
     "RadixSortError", "load_library", "library_path", "temp_bytes", "radix_sort_keys",
     "radix_sort_pairs", "segmented_sort", "segmented_temp_bytes", "upfront_histograms",
-    "device_status", "passes_run", "set_pass_skipping", "set_tile_offsets", "set_small_sort",
-    "SMALL_SORT_MAX_KEYS", "copy_probe", "set_lookback_timeout_ns", "lookback_timeout_probe",
-    "profile_enable", "profile_read", "launch_count_reset", "EXPORTED_SYMBOLS",
+    "device_status", "passes_run", "SMALL_SORT_MAX_KEYS", "copy_probe",
+    "lookback_timeout_probe", "profile_enable", "profile_read", "launch_count_reset",
+    "noalloc_status", "EXPORTED_SYMBOLS", "RS_MAX_KEYS", "RS_MAX_ROW_KEYS",
 ]
 
 RS_OK, RS_ERR_INVALID, RS_ERR_TEMP_TOO_SMALL, RS_ERR_CUDA, RS_ERR_LOOKBACK_TIMEOUT = range(5)
 RS_F16, RS_BF16 = 0, 1
 KEY_TYPES = {"u32": (0, 4), "i32": (1, 4), "f32": (2, 4), "u64": (3, 8), "i64": (4, 8),
              "f64": (5, 8)}
-RS_MAX_KEYS = (1 << 30) - 1
+RS_MAX_KEYS = (1 << 32) - 1       # one flat sort
+RS_MAX_ROW_KEYS = (1 << 30) - 1   # one row of a row-wise sort
+RS_OPT_PASS_SKIPPING, RS_OPT_TILE_OFFSETS, RS_OPT_NO_SMALL_SORT = 0x1, 0x2, 0x4
 # Rows (or flat inputs) of at most this many keys, with 4- or 8-bit digits,
-# are sorted by one kernel that runs every pass in shared memory (unless
-# set_small_sort(False)); it runs every pass, pass skipping included.
+# are sorted by one kernel that runs every pass in shared memory (unless a
+# call passes small_sort=False); it runs every pass, pass skipping included.
 SMALL_SORT_MAX_KEYS = 8192
 KERNEL_NAMES = {0: "upfront_hist", 1: "digit_scan", 2: "onesweep", 3: "copy_probe",
                 4: "timeout_probe", 5: "finish", 6: "tile_counts",
                 7: "small_sort"}
 
 EXPORTED_SYMBOLS = (
-    "radix_sort_temp_bytes", "radix_sort_keys_u32", "radix_sort_keys_u64",
+    "radix_sort_keys_temp_bytes", "radix_sort_keys_u32", "radix_sort_keys_u64",
     "radix_sort_pairs_u32", "radix_sort_pairs_u64", "radix_segmented_sort_temp_bytes",
-    "radix_segmented_sort_f16", "radix_sort_histograms", "radix_sort_device_status",
-    "rs_status_string", "rs_set_lookback_timeout_ns", "rs_lookback_timeout_probe",
+    "radix_segmented_sort_f16", "radix_segmented_sort_f16_ex", "radix_sort_histograms",
+    "radix_sort_device_status", "rs_status_string", "rs_lookback_timeout_probe",
     "rs_copy_probe", "rs_profile_enable", "rs_profile_read", "rs_launch_count_reset",
-    "radix_sort_pairs_u32_noalloc", "radix_sort_keys_typed", "radix_sort_pairs_typed",
-    "radix_sort_passes_run", "rs_set_pass_skipping", "rs_set_tile_offsets", "rs_set_small_sort",
+    "radix_sort_pairs_u32_noalloc", "radix_sort_pairs_u32_noalloc_status",
+    "radix_sort_keys_typed", "radix_sort_pairs_typed", "radix_sort_passes_run",
 )
 
 
@@ -60,6 +66,21 @@ class RadixSortError(RuntimeError):
 
 class KernelTime(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("ms", ctypes.c_float), ("units", ctypes.c_uint64)]
+
+
+class Options(ctypes.Structure):
+    """struct rs_options of include/lsdrs.h."""
+    _fields_ = [("flags", ctypes.c_uint), ("lookback_timeout_ns", ctypes.c_uint64)]
+
+
+def _options(pass_skipping=False, tile_offsets=False, small_sort=True, lookback_timeout_ns=0):
+    """An rs_options for the call, or None when every option is at its default."""
+    flags = ((RS_OPT_PASS_SKIPPING if pass_skipping else 0)
+             | (RS_OPT_TILE_OFFSETS if tile_offsets else 0)
+             | (0 if small_sort else RS_OPT_NO_SMALL_SORT))
+    if not flags and not lookback_timeout_ns:
+        return None
+    return Options(flags, int(lookback_timeout_ns))
 
 
 _lock = threading.Lock()
@@ -91,26 +112,24 @@ def load_library() -> ctypes.CDLL:
                               ctypes.c_uint64)
         st = ctypes.c_int
         sig = {
-            "radix_sort_temp_bytes": [sz, i, i, i, i, i, P],
+            "radix_sort_keys_temp_bytes": [sz, i, i, i, i, i, P],
             "radix_sort_keys_u32": [P, P, sz, i, i, i, P, sz, P],
             "radix_sort_keys_u64": [P, P, sz, i, i, i, P, sz, P],
             "radix_sort_pairs_u32": [P, P, P, P, sz, i, i, i, P, sz, P],
             "radix_sort_pairs_u64": [P, P, P, P, sz, i, i, i, P, sz, P],
             "radix_segmented_sort_temp_bytes": [i64, i64, P],
             "radix_segmented_sort_f16": [P, P, P, i64, i64, i, i, P, sz, P],
+            "radix_segmented_sort_f16_ex": [P, P, P, i64, i64, i, i, P, sz, P, P],
             "radix_sort_histograms": [P, i, sz, i, i, i, P, P, P, sz, P],
             "radix_sort_device_status": [P, P],
-            "rs_set_lookback_timeout_ns": [u64],
             "rs_lookback_timeout_probe": [P, u64, P, P],
             "rs_copy_probe": [P, P, sz, P],
             "rs_profile_enable": [i],
             "radix_sort_pairs_u32_noalloc": [P, P, P, P, sz, i, i, i, P],
-            "radix_sort_keys_typed": [i, i, P, P, sz, i, i, i, P, sz, P],
+            "radix_sort_pairs_u32_noalloc_status": [P],
+            "radix_sort_keys_typed": [i, i, P, P, sz, i, i, i, P, sz, P, P],
             "radix_sort_passes_run": [P, P, P],
-            "rs_set_pass_skipping": [i],
-            "rs_set_tile_offsets": [i],
-            "rs_set_small_sort": [i],
-            "radix_sort_pairs_typed": [i, i, P, P, P, P, sz, i, i, i, P, sz, P],
+            "radix_sort_pairs_typed": [i, i, P, P, P, P, sz, i, i, i, P, sz, P, P],
         }
         for name, args in sig.items():
             f = getattr(lib, name)
@@ -178,9 +197,9 @@ def _require_cuda(*ts):
 def temp_bytes(n: int, key_bytes: int, value_bytes: int, begin_bit: int, end_bit: int,
                digit_bits: int) -> int:
     out = ctypes.c_size_t(0)
-    _check(load_library().radix_sort_temp_bytes(n, key_bytes, value_bytes, begin_bit, end_bit,
-                                                digit_bits, ctypes.byref(out)),
-           "radix_sort_temp_bytes")
+    _check(load_library().radix_sort_keys_temp_bytes(n, key_bytes, value_bytes, begin_bit,
+                                                     end_bit, digit_bits, ctypes.byref(out)),
+           "radix_sort_keys_temp_bytes")
     return out.value
 
 
@@ -215,10 +234,12 @@ def _key_type(key_type, kb: int, descending: bool):
 
 def radix_sort_keys(keys, out=None, begin_bit: int = 0, end_bit: int | None = None,
                     digit_bits: int = 8, temp=None, stream=None, key_type=None,
-                    descending: bool = False):
+                    descending: bool = False, pass_skipping: bool = False,
+                    small_sort: bool = True, lookback_timeout_ns: int = 0):
     """Stable sort of the bits [begin_bit, end_bit) of ``keys``: unsigned and
     ascending by default; ``key_type`` and ``descending`` select the typed
-    sort (the bits then belong to the order-preserving transform)."""
+    sort (the bits then belong to the order-preserving transform).  The
+    keyword options are those of struct rs_options (include/lsdrs.h)."""
     import torch
     lib = load_library()
     keys = keys.reshape(-1)
@@ -231,6 +252,9 @@ def radix_sort_keys(keys, out=None, begin_bit: int = 0, end_bit: int | None = No
     _require_cuda(out)
     n = keys.numel()
     code, _ = _key_type(key_type, kb, descending)
+    opts = _options(pass_skipping, False, small_sort, lookback_timeout_ns)
+    if opts is not None and code is None:
+        code = KEY_TYPES["u32" if kb == 4 else "u64"][0]
     tb = temp_bytes(n, kb, 0, begin_bit, end_bit, digit_bits)
     t = _temp(tb, keys.device, temp)
     tsz = t.numel() * t.element_size()
@@ -240,16 +264,19 @@ def radix_sort_keys(keys, out=None, begin_bit: int = 0, end_bit: int | None = No
                _stream_ptr(stream))
     else:
         st = lib.radix_sort_keys_typed(code, int(descending), _ptr(keys), _ptr(out), n, begin_bit,
-                                       end_bit, digit_bits, _ptr(t), tsz, _stream_ptr(stream))
+                                       end_bit, digit_bits, _ptr(t), tsz,
+                                       ctypes.byref(opts) if opts is not None else None,
+                                       _stream_ptr(stream))
     _check(st, "radix_sort_keys")
     return out
 
 
 def radix_sort_pairs(keys, values, keys_out=None, values_out=None, begin_bit: int = 0,
                      end_bit: int | None = None, digit_bits: int = 8, temp=None, stream=None,
-                     key_type=None, descending: bool = False):
+                     key_type=None, descending: bool = False, pass_skipping: bool = False,
+                     small_sort: bool = True, lookback_timeout_ns: int = 0):
     """Stable key-value sort: 4-byte ``values`` follow their keys (key order
-    as for radix_sort_keys)."""
+    and options as for radix_sort_keys)."""
     import torch
     lib = load_library()
     keys = keys.reshape(-1)
@@ -266,6 +293,9 @@ def radix_sort_pairs(keys, values, keys_out=None, values_out=None, begin_bit: in
     _require_cuda(keys_out, values_out)
     n = keys.numel()
     code, _ = _key_type(key_type, kb, descending)
+    opts = _options(pass_skipping, False, small_sort, lookback_timeout_ns)
+    if opts is not None and code is None:
+        code = KEY_TYPES["u32" if kb == 4 else "u64"][0]
     tb = temp_bytes(n, kb, 4, begin_bit, end_bit, digit_bits)
     t = _temp(tb, keys.device, temp)
     tsz = t.numel() * t.element_size()
@@ -276,18 +306,25 @@ def radix_sort_pairs(keys, values, keys_out=None, values_out=None, begin_bit: in
     else:
         st = lib.radix_sort_pairs_typed(code, int(descending), _ptr(keys), _ptr(keys_out),
                                         _ptr(values), _ptr(values_out), n, begin_bit, end_bit,
-                                        digit_bits, _ptr(t), tsz, _stream_ptr(stream))
+                                        digit_bits, _ptr(t), tsz,
+                                        ctypes.byref(opts) if opts is not None else None,
+                                        _stream_ptr(stream))
     _check(st, "radix_sort_pairs")
     return keys_out, values_out
 
 
 def segmented_sort(x, descending: bool = False, values_out=None, indices_out=None,
-                   temp=None, stream=None):
+                   temp=None, stream=None, tile_offsets: bool = False,
+                   pass_skipping: bool = False, small_sort: bool = True,
+                   lookback_timeout_ns: int = 0):
     """Row-wise stable sort of a 2-D float16/bfloat16 tensor along the last dim.
 
     Returns (sorted values, int64 indices), like ``torch.sort(x, dim=-1)``
     with ties in input order, -0 before +0 ascending and NaNs placed by sign
     (negative NaNs first, positive NaNs last; reversed when descending).
+    ``tile_offsets`` precomputes each tile's output offsets before every
+    pass instead of the look-back; the other options are as for
+    radix_sort_keys.
     """
     import torch
     lib = load_library()
@@ -310,10 +347,17 @@ def segmented_sort(x, descending: bool = False, values_out=None, indices_out=Non
     _require_cuda(vals, idx)
     tb = segmented_temp_bytes(rows, cols)
     t = _temp(tb, x.device, temp)
-    _check(lib.radix_segmented_sort_f16(_ptr(x), _ptr(vals), _ptr(idx), rows, cols, kind,
-                                        int(bool(descending)), _ptr(t),
-                                        t.numel() * t.element_size(), _stream_ptr(stream)),
-           "radix_segmented_sort_f16")
+    opts = _options(pass_skipping, tile_offsets, small_sort, lookback_timeout_ns)
+    if opts is None:
+        st = lib.radix_segmented_sort_f16(_ptr(x), _ptr(vals), _ptr(idx), rows, cols, kind,
+                                          int(bool(descending)), _ptr(t),
+                                          t.numel() * t.element_size(), _stream_ptr(stream))
+    else:
+        st = lib.radix_segmented_sort_f16_ex(_ptr(x), _ptr(vals), _ptr(idx), rows, cols, kind,
+                                             int(bool(descending)), _ptr(t),
+                                             t.numel() * t.element_size(), ctypes.byref(opts),
+                                             _stream_ptr(stream))
+    _check(st, "radix_segmented_sort_f16")
     return vals, idx
 
 
@@ -339,24 +383,6 @@ def upfront_histograms(keys, begin_bit: int = 0, end_bit: int | None = None,
     return hist[:passes], bases[:passes]
 
 
-def set_tile_offsets(precomputed: bool):
-    """Row-wise sorts: precompute each tile's output offsets before every pass
-    (True) instead of the decoupled look-back (False, the default)."""
-    _check(load_library().rs_set_tile_offsets(int(bool(precomputed))), "rs_set_tile_offsets")
-
-
-def set_pass_skipping(on: bool):
-    """Skip identity passes (every key with the same digit) from now on
-    (process-wide; off by default)."""
-    _check(load_library().rs_set_pass_skipping(int(bool(on))), "rs_set_pass_skipping")
-
-
-def set_small_sort(on: bool):
-    """Sort rows of at most SMALL_SORT_MAX_KEYS keys in one kernel from now
-    on (process-wide; on by default); off, they take the multi-kernel path."""
-    _check(load_library().rs_set_small_sort(int(bool(on))), "rs_set_small_sort")
-
-
 def passes_run(temp, stream=None) -> int:
     """Passes the last sort with this scratch buffer ran (identity passes,
     where every key has the same digit, are skipped).  Synchronises."""
@@ -379,10 +405,6 @@ def copy_probe(dst, src, stream=None):
     _require_cuda(dst, src)
     _check(load_library().rs_copy_probe(_ptr(dst), _ptr(src), nbytes, _stream_ptr(stream)),
            "rs_copy_probe")
-
-
-def set_lookback_timeout_ns(ns: int):
-    _check(load_library().rs_set_lookback_timeout_ns(int(ns)), "rs_set_lookback_timeout_ns")
 
 
 def lookback_timeout_probe(timeout_ns: int, stream=None) -> int:
@@ -410,3 +432,9 @@ def profile_read(max_records: int = 1 << 16):
 
 def launch_count_reset() -> int:
     return int(load_library().rs_launch_count_reset())
+
+
+def noalloc_status(stream=None) -> int:
+    """Synchronise and return the device-side status of the last no-allocation
+    sort enqueued on the current device (radix_sort_pairs_u32_noalloc_status)."""
+    return int(load_library().radix_sort_pairs_u32_noalloc_status(_stream_ptr(stream)))

@@ -1,6 +1,7 @@
 // The C ABI (include/lsdrs.h): argument checks, the scratch layout, the pass
 // schedule and the launches.  Everything here runs on the host; each sort
 // enqueues K-HIST, K-SCAN and one K-SWEEP per pass on the caller's stream.
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -13,11 +14,11 @@ using namespace lsdrs;
 
 namespace {
 
-std::atomic<uint64_t> g_timeout_ns{2000000000ull};
 std::atomic<uint64_t> g_launches{0};
-std::atomic<int> g_pass_skipping{0};
-std::atomic<int> g_small_sort{1};
-std::atomic<int> g_tile_offsets{0};
+
+// Default and largest limit on one look-back or copy wait inside a kernel.
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+constexpr uint64_t kMaxTimeoutNs = 60000000000ull;
 
 // ---------------------------------------------------------------- profiling
 struct ProfRec {
@@ -54,11 +55,37 @@ cudaError_t timed_launch(int kernel, uint64_t units, cudaStream_t s, F&& launch)
   return e;
 }
 
+// Per-call options (rs_options), resolved against the defaults.
+struct Options {
+  bool pass_skipping = false;
+  bool tile_offsets = false;
+  bool small_sort = true;
+  uint64_t timeout_ns = kDefaultTimeoutNs;
+};
+
+constexpr unsigned kKnownFlags = RS_OPT_PASS_SKIPPING | RS_OPT_TILE_OFFSETS | RS_OPT_NO_SMALL_SORT;
+
+bool resolve_options(const rs_options* o, Options* out) {
+  Options r;
+  if (o != nullptr) {
+    if (o->flags & ~kKnownFlags) return false;
+    r.pass_skipping = (o->flags & RS_OPT_PASS_SKIPPING) != 0;
+    r.tile_offsets = (o->flags & RS_OPT_TILE_OFFSETS) != 0;
+    r.small_sort = (o->flags & RS_OPT_NO_SMALL_SORT) == 0;
+    if (o->lookback_timeout_ns != 0) {
+      if (o->lookback_timeout_ns > kMaxTimeoutNs) return false;
+      r.timeout_ns = o->lookback_timeout_ns;
+    }
+  }
+  *out = r;
+  return true;
+}
+
 // -------------------------------------------------------------------- plan
 // Scratch layout (offsets in bytes from `temp`, each 256-byte aligned):
 //   header   : device error word, tile counters, pass schedule (kernels.h)
-//   status0  : look-back words of even passes  [tiles][radix] u32
-//   status1  : look-back words of odd passes   [tiles][radix] u32
+//   status0  : look-back words of even passes  [tiles][radix] u32 (u64 from 2^30 keys)
+//   status1  : look-back words of odd passes   [tiles][radix]
 //   bases    : [rows][passes][radix] u32
 //   slots    : [rows][hist chunks][passes][radix] u32 partial histograms
 //   alt_keys : ping-pong key buffer
@@ -76,11 +103,16 @@ struct Plan {
   uint32_t last_mask;
   int tile;
   int64_t tiles_per_row, tiles;
+  int status_word;           // bytes per look-back word: 4, or 8 from 2^30 keys
+  int64_t max_chunks;        // histogram slots reserved per row
+  // set per call by configure(): histogram chunks for the device's SMs
   int chunks_per_row;
   int64_t chunk_len;
   size_t off_status0, off_status1, off_bases, off_slots, off_tile_offsets, off_alt_keys,
       off_alt_vals, total;
 };
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 rs_status make_plan(KeyKind key, ValKind val, int64_t rows, int64_t cols, int begin_bit,
                     int end_bit, int bits, Plan* out) {
@@ -89,7 +121,11 @@ rs_status make_plan(KeyKind key, ValKind val, int64_t rows, int64_t cols, int be
   p.val = val;
   p.key_bytes = (key == kKeyU32 || key == kKeyX32) ? 4 : (key == kKeyU64 || key == kKeyX64) ? 8 : 2;
   const int kbits = p.key_bytes * 8;
-  if (rows < 0 || cols < 0 || static_cast<uint64_t>(cols) > RS_MAX_KEYS) return RS_ERR_INVALID;
+  if (rows < 0 || cols < 0) return RS_ERR_INVALID;
+  // a flat sort (one row) may hold up to RS_MAX_KEYS keys; a row of a
+  // row-wise sort up to RS_MAX_ROW_KEYS (its column indices are int32 inside)
+  const bool flat = rows == 1 && val != kValIdx;
+  if (static_cast<uint64_t>(cols) > (flat ? RS_MAX_KEYS : RS_MAX_ROW_KEYS)) return RS_ERR_INVALID;
   // every row is at least one tile, and tile ids are 24 bits (this also keeps
   // rows * tiles_per_row and rows * cols far from overflowing)
   if (rows > static_cast<int64_t>(kTileMask)) return RS_ERR_INVALID;
@@ -106,30 +142,27 @@ rs_status make_plan(KeyKind key, ValKind val, int64_t rows, int64_t cols, int be
   const int last_w = end_bit - (begin_bit + (p.passes - 1) * bits);
   p.last_mask = (1u << last_w) - 1u;
   p.tile = sweep_shape(key, val).tile();
-  p.tiles_per_row = (cols + p.tile - 1) / p.tile;
+  p.tiles_per_row = cdiv(cols, p.tile);
   p.tiles = rows * p.tiles_per_row;
   if (p.tiles > static_cast<int64_t>(kTileMask)) return RS_ERR_INVALID;  // tile ids: 24 bits
-  // K-HIST chunking: enough CTAs to fill the GPU, at least kHistMinChunk keys each.
-  int64_t want = rows > 0 ? (kHistTargetCtas + rows - 1) / rows : 1;
-  int64_t max_chunks = (cols + kHistMinChunk - 1) / kHistMinChunk;
-  if (max_chunks < 1) max_chunks = 1;
-  if (want > max_chunks) want = max_chunks;
-  if (want < 1) want = 1;
-  p.chunks_per_row = static_cast<int>(want);
-  p.chunk_len = (cols + want - 1) / want;
-  p.chunk_len = static_cast<int64_t>(align_up(static_cast<size_t>(p.chunk_len), 64));
+  // A look-back count reaches the row length: 32-bit words hold 30 bits.
+  p.status_word = cols > kMaxNarrowKeys ? 8 : 4;
+  // histogram slots for the chunks of any device configure() may see
+  p.max_chunks = rows > 0 ? cdiv(kMaxHistCtas, rows) : 1;
 
-  const size_t status_bytes = align_up(static_cast<size_t>(p.tiles) * p.radix * 4, 256);
+  const size_t status_bytes =
+      align_up(static_cast<size_t>(p.tiles) * p.radix * p.status_word, 256);
   const size_t n = static_cast<size_t>(rows) * static_cast<size_t>(cols);
+  const size_t pr = static_cast<size_t>(p.passes) * p.radix * 4;
   size_t off = kHeaderBytes;
   p.off_status0 = off;
   off += status_bytes;
   p.off_status1 = off;
   off += status_bytes;
   p.off_bases = off;
-  off += align_up(static_cast<size_t>(rows) * p.passes * p.radix * 4, 256);
+  off += align_up(static_cast<size_t>(rows) * pr, 256);
   p.off_slots = off;
-  off += align_up(static_cast<size_t>(rows) * p.chunks_per_row * p.passes * p.radix * 4, 256);
+  off += align_up(static_cast<size_t>(rows) * p.max_chunks * pr, 256);
   p.off_tile_offsets = off;  // row-wise sorts: precomputed tile offsets of one pass
   if (val == kValIdx) off += align_up(static_cast<size_t>(p.tiles) * p.radix * 4, 256);
   p.off_alt_keys = off;
@@ -141,6 +174,18 @@ rs_status make_plan(KeyKind key, ValKind val, int64_t rows, int64_t cols, int be
   return RS_OK;
 }
 
+// Per call: the K-HIST chunks, one CTA per SM of the device (at most
+// kMaxHistCtas), each at least kHistMinChunk keys.
+void configure(Plan* p) {
+  const int64_t sms = std::min<int64_t>(device_sm_count(), kMaxHistCtas);
+  int64_t want = p->rows > 0 ? cdiv(sms, p->rows) : 1;
+  want = std::min<int64_t>(want, std::max<int64_t>(1, cdiv(p->cols, kHistMinChunk)));
+  want = std::max<int64_t>(want, 1);
+  p->chunks_per_row = static_cast<int>(want);
+  p->chunk_len = static_cast<int64_t>(
+      align_up(static_cast<size_t>(std::max<int64_t>(1, cdiv(p->cols, want))), 64));
+}
+
 inline unsigned char* at(void* temp, size_t off) { return static_cast<unsigned char*>(temp) + off; }
 
 bool overlap(const void* a, size_t an, const void* b, size_t bn) {
@@ -148,7 +193,8 @@ bool overlap(const void* a, size_t an, const void* b, size_t bn) {
   return x < y + bn && y < x + an;
 }
 
-// Enqueue K-HIST and K-SCAN.  hist_out: optional copy of the totals.
+// Enqueue K-HIST and K-SCAN.  hist_out / bases_out: optional copies of the
+// rows' totals and bases ([rows][passes][radix]).
 rs_status run_front(const Plan& p, const void* keys, const KeyXform& xf, void* temp,
                     uint32_t* hist_out, uint32_t* bases_out, bool in_place, bool dynamic,
                     cudaStream_t s) {
@@ -178,7 +224,8 @@ rs_status run_front(const Plan& p, const void* keys, const KeyXform& xf, void* t
   c.passes = p.passes;
   c.radix = p.radix;
   c.hist_out = hist_out;
-  c.bases = bases_out ? bases_out : reinterpret_cast<uint32_t*>(at(temp, p.off_bases));
+  c.bases_out = bases_out;
+  c.bases = reinterpret_cast<uint32_t*>(at(temp, p.off_bases));
   c.header = reinterpret_cast<uint32_t*>(temp);
   c.cols = p.cols;
   c.in_place = in_place ? 1 : 0;
@@ -189,6 +236,15 @@ rs_status run_front(const Plan& p, const void* keys, const KeyXform& xf, void* t
 }
 
 cudaError_t sweep(const Plan& p, const SweepArgs& a, int* launched, cudaStream_t s) {
+  if (a.wide) {
+    switch (p.key) {
+      case kKeyU32: return launch_sweep_u32_wide(p.val, p.bits, a, launched, s);
+      case kKeyU64: return launch_sweep_u64_wide(p.val, p.bits, a, launched, s);
+      case kKeyX32: return launch_sweep_x32_wide(p.val, p.bits, a, launched, s);
+      case kKeyX64: return launch_sweep_x64_wide(p.val, p.bits, a, launched, s);
+      default: return cudaErrorInvalidValue;  // rows stay below 2^30 keys
+    }
+  }
   switch (p.key) {
     case kKeyU32: return launch_sweep_u32(p.val, p.bits, a, launched, s);
     case kKeyU64: return launch_sweep_u64(p.val, p.bits, a, launched, s);
@@ -202,9 +258,9 @@ cudaError_t sweep(const Plan& p, const SweepArgs& a, int* launched, cudaStream_t
 // A whole sort: front stages, then one sweep per pass.  The pass that
 // writes `keys_out` last is chosen by parity so that no copy is needed,
 // except for an in-place sort with an odd number of passes.
-rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const void* vals_in,
+rs_status run_sort(Plan p, const void* keys_in, void* keys_out, const void* vals_in,
                    void* vals_out, const KeyXform& xf, void* temp, size_t temp_bytes,
-                   cudaStream_t s) {
+                   const Options& opt, cudaStream_t s) {
   const size_t n = static_cast<size_t>(p.rows) * static_cast<size_t>(p.cols);
   if (n == 0) return RS_OK;
   if (temp == nullptr) return RS_ERR_INVALID;
@@ -241,8 +297,7 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
   if (p.val == kValIdx && p.passes > 2) return RS_ERR_INVALID;  // 16-bit keys: two passes
 
   // rows of at most one small tile: the whole sort in one kernel
-  if (g_small_sort.load(std::memory_order_relaxed) != 0 &&
-      small_sort_fits(p.key, p.val, p.bits, p.cols)) {
+  if (opt.small_sort && small_sort_fits(p.key, p.val, p.bits, p.cols)) {
     SmallArgs sa{};
     sa.keys_in = keys_in;
     sa.keys_out = keys_out;
@@ -263,8 +318,9 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
 
   // row-wise sorts may take precomputed tile offsets instead of the
   // look-back; that mode keeps the static schedule (every pass runs)
-  const bool precomputed = p.val == kValIdx && g_tile_offsets.load(std::memory_order_relaxed) != 0;
-  const bool dynamic = !precomputed && g_pass_skipping.load(std::memory_order_relaxed) != 0;
+  const bool precomputed = p.val == kValIdx && opt.tile_offsets;
+  const bool dynamic = !precomputed && opt.pass_skipping;
+  configure(&p);
   rs_status st = run_front(p, keys_in, xf, temp, nullptr, nullptr, in_place, dynamic, s);
   if (st != RS_OK) return st;
 
@@ -282,8 +338,9 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
   a.vals[kBufIn] = p.val == kValU32 ? vals_in : nullptr;
   a.vals[kBufAlt] = p.val == kValNone ? nullptr : alt_vals;
   a.vals[kBufOut] = vals_out;
-  a.status_arr[0] = reinterpret_cast<uint32_t*>(at(temp, p.off_status0));
-  a.status_arr[1] = reinterpret_cast<uint32_t*>(at(temp, p.off_status1));
+  a.status_arr[0] = at(temp, p.off_status0);
+  a.status_arr[1] = at(temp, p.off_status1);
+  a.wide = p.status_word == 8 ? 1 : 0;
   a.rows = p.rows;
   a.cols = p.cols;
   a.tiles_per_row = p.tiles_per_row;
@@ -291,7 +348,7 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
   a.xf = xf;
   a.bases_row_stride = static_cast<int64_t>(p.passes) * p.radix;
   a.error = header + kHdrError;
-  a.timeout_ns = g_timeout_ns.load(std::memory_order_relaxed);
+  a.timeout_ns = opt.timeout_ns;
   a.dynamic = dynamic ? 1 : 0;
   uint32_t prev = kBufIn;
   for (int q = 0; q < p.passes; ++q) {
@@ -313,6 +370,8 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
     a.pass_status_zero = last ? nullptr : a.status_arr[(q + 1) & 1];
     a.shift = p.begin_bit + q * p.bits;
     a.mask = last ? p.last_mask : static_cast<uint32_t>(p.radix - 1);
+    a.byte_sel = 0x4440u | static_cast<uint32_t>((a.shift >> 3) & 3);
+    a.byte_hi = (a.shift >> 3) >= 4 ? 1 : 0;
     a.bases = bases + static_cast<size_t>(q) * p.radix;
     a.tile_counter = header + kHdrTileCounter + q;
     if (precomputed) {
@@ -364,14 +423,15 @@ rs_status run_sort(const Plan& p, const void* keys_in, void* keys_out, const voi
 }
 
 rs_status flat_sort(KeyKind key, const KeyXform& xf, ValKind val, const void* ki, void* ko,
-                    const void* vi, void* vo,
-                    size_t n, int begin_bit, int end_bit, int bits, void* temp,
-                    size_t temp_bytes, void* stream) {
+                    const void* vi, void* vo, size_t n, int begin_bit, int end_bit, int bits,
+                    void* temp, size_t temp_bytes, const rs_options* opts, void* stream) {
   if (n > RS_MAX_KEYS) return RS_ERR_INVALID;
+  Options o;
+  if (!resolve_options(opts, &o)) return RS_ERR_INVALID;
   Plan p;
   rs_status st = make_plan(key, val, 1, static_cast<int64_t>(n), begin_bit, end_bit, bits, &p);
   if (st != RS_OK) return st;
-  return run_sort(p, ki, ko, vi, vo, xf, temp, temp_bytes, static_cast<cudaStream_t>(stream));
+  return run_sort(p, ki, ko, vi, vo, xf, temp, temp_bytes, o, static_cast<cudaStream_t>(stream));
 }
 
 // The key kind and transform of a typed global sort (see keys.cuh): unsigned
@@ -404,8 +464,8 @@ bool typed_key(rs_key_type type, int descending, KeyKind* kind, KeyXform* xf) {
 
 extern "C" {
 
-rs_status radix_sort_temp_bytes(size_t n, int key_bytes, int value_bytes, int begin_bit,
-                                int end_bit, int digit_bits, size_t* bytes) {
+rs_status radix_sort_keys_temp_bytes(size_t n, int key_bytes, int value_bytes, int begin_bit,
+                                     int end_bit, int digit_bits, size_t* bytes) {
   if (!bytes || n > RS_MAX_KEYS) return RS_ERR_INVALID;
   if (key_bytes != 4 && key_bytes != 8) return RS_ERR_INVALID;
   if (value_bytes != 0 && value_bytes != 4) return RS_ERR_INVALID;
@@ -421,14 +481,14 @@ rs_status radix_sort_keys_u32(const uint32_t* keys_in, uint32_t* keys_out, size_
                               int begin_bit, int end_bit, int digit_bits, void* temp,
                               size_t temp_bytes, void* stream) {
   return flat_sort(kKeyU32, KeyXform{0, 0}, kValNone, keys_in, keys_out, nullptr, nullptr, n,
-                   begin_bit, end_bit, digit_bits, temp, temp_bytes, stream);
+                   begin_bit, end_bit, digit_bits, temp, temp_bytes, nullptr, stream);
 }
 
 rs_status radix_sort_keys_u64(const uint64_t* keys_in, uint64_t* keys_out, size_t n,
                               int begin_bit, int end_bit, int digit_bits, void* temp,
                               size_t temp_bytes, void* stream) {
   return flat_sort(kKeyU64, KeyXform{0, 0}, kValNone, keys_in, keys_out, nullptr, nullptr, n,
-                   begin_bit, end_bit, digit_bits, temp, temp_bytes, stream);
+                   begin_bit, end_bit, digit_bits, temp, temp_bytes, nullptr, stream);
 }
 
 rs_status radix_sort_pairs_u32(const uint32_t* keys_in, uint32_t* keys_out,
@@ -436,7 +496,7 @@ rs_status radix_sort_pairs_u32(const uint32_t* keys_in, uint32_t* keys_out,
                                int begin_bit, int end_bit, int digit_bits, void* temp,
                                size_t temp_bytes, void* stream) {
   return flat_sort(kKeyU32, KeyXform{0, 0}, kValU32, keys_in, keys_out, vals_in, vals_out, n,
-                   begin_bit, end_bit, digit_bits, temp, temp_bytes, stream);
+                   begin_bit, end_bit, digit_bits, temp, temp_bytes, nullptr, stream);
 }
 
 rs_status radix_sort_pairs_u64(const uint64_t* keys_in, uint64_t* keys_out,
@@ -444,28 +504,29 @@ rs_status radix_sort_pairs_u64(const uint64_t* keys_in, uint64_t* keys_out,
                                int begin_bit, int end_bit, int digit_bits, void* temp,
                                size_t temp_bytes, void* stream) {
   return flat_sort(kKeyU64, KeyXform{0, 0}, kValU32, keys_in, keys_out, vals_in, vals_out, n,
-                   begin_bit, end_bit, digit_bits, temp, temp_bytes, stream);
+                   begin_bit, end_bit, digit_bits, temp, temp_bytes, nullptr, stream);
 }
 
 rs_status radix_sort_keys_typed(rs_key_type type, int descending, const void* keys_in,
                                 void* keys_out, size_t n, int begin_bit, int end_bit,
-                                int digit_bits, void* temp, size_t temp_bytes, void* stream) {
+                                int digit_bits, void* temp, size_t temp_bytes,
+                                const rs_options* opts, void* stream) {
   KeyKind kind;
   KeyXform xf;
   if (!typed_key(type, descending, &kind, &xf)) return RS_ERR_INVALID;
   return flat_sort(kind, xf, kValNone, keys_in, keys_out, nullptr, nullptr, n, begin_bit, end_bit,
-                   digit_bits, temp, temp_bytes, stream);
+                   digit_bits, temp, temp_bytes, opts, stream);
 }
 
 rs_status radix_sort_pairs_typed(rs_key_type type, int descending, const void* keys_in,
                                  void* keys_out, const uint32_t* vals_in, uint32_t* vals_out,
                                  size_t n, int begin_bit, int end_bit, int digit_bits, void* temp,
-                                 size_t temp_bytes, void* stream) {
+                                 size_t temp_bytes, const rs_options* opts, void* stream) {
   KeyKind kind;
   KeyXform xf;
   if (!typed_key(type, descending, &kind, &xf)) return RS_ERR_INVALID;
   return flat_sort(kind, xf, kValU32, keys_in, keys_out, vals_in, vals_out, n, begin_bit, end_bit,
-                   digit_bits, temp, temp_bytes, stream);
+                   digit_bits, temp, temp_bytes, opts, stream);
 }
 
 rs_status radix_segmented_sort_temp_bytes(int64_t rows, int64_t cols, size_t* bytes) {
@@ -477,19 +538,29 @@ rs_status radix_segmented_sort_temp_bytes(int64_t rows, int64_t cols, size_t* by
   return RS_OK;
 }
 
-rs_status radix_segmented_sort_f16(const uint16_t* in, uint16_t* vals_out, int64_t* idx_out,
-                                   int64_t rows, int64_t cols, rs_float_kind kind,
-                                   int descending, void* temp, size_t temp_bytes,
-                                   void* stream) {
+rs_status radix_segmented_sort_f16_ex(const uint16_t* in, uint16_t* vals_out, int64_t* idx_out,
+                                      int64_t rows, int64_t cols, rs_float_kind kind,
+                                      int descending, void* temp, size_t temp_bytes,
+                                      const rs_options* opts, void* stream) {
   if (kind != RS_F16 && kind != RS_BF16) return RS_ERR_INVALID;
   if (descending != 0 && descending != 1) return RS_ERR_INVALID;
+  Options o;
+  if (!resolve_options(opts, &o)) return RS_ERR_INVALID;
   Plan p;
   rs_status st = make_plan(kKeyF16, kValIdx, rows, cols, 0, 16, 8, &p);
   if (st != RS_OK) return st;
   // 16-bit float bijection; descending complements it
   const uint64_t flip = descending ? 0xFFFFu : 0u;
-  return run_sort(p, in, vals_out, nullptr, idx_out, KeyXform{0x8000u ^ flip, 0xFFFFu ^ flip}, temp,
-                  temp_bytes, static_cast<cudaStream_t>(stream));
+  return run_sort(p, in, vals_out, nullptr, idx_out, KeyXform{0x8000u ^ flip, 0xFFFFu ^ flip},
+                  temp, temp_bytes, o, static_cast<cudaStream_t>(stream));
+}
+
+rs_status radix_segmented_sort_f16(const uint16_t* in, uint16_t* vals_out, int64_t* idx_out,
+                                   int64_t rows, int64_t cols, rs_float_kind kind,
+                                   int descending, void* temp, size_t temp_bytes,
+                                   void* stream) {
+  return radix_segmented_sort_f16_ex(in, vals_out, idx_out, rows, cols, kind, descending, temp,
+                                     temp_bytes, nullptr, stream);
 }
 
 rs_status radix_sort_histograms(const void* keys, int key_bytes, size_t n, int begin_bit,
@@ -506,6 +577,7 @@ rs_status radix_sort_histograms(const void* keys, int key_bytes, size_t n, int b
   if (n > 0 && !keys) return RS_ERR_INVALID;
   if (temp_bytes < p.total) return RS_ERR_TEMP_TOO_SMALL;
   if (reinterpret_cast<uintptr_t>(temp) % 256 != 0) return RS_ERR_INVALID;
+  configure(&p);
   return run_front(p, keys, KeyXform{0, 0}, temp, hist_out, bases_out, false, false,
                    static_cast<cudaStream_t>(stream));
 }
@@ -543,33 +615,9 @@ const char* rs_status_string(rs_status status) {
   return "RS_UNKNOWN";
 }
 
-rs_status rs_set_pass_skipping(int on) {
-  if (on != 0 && on != 1) return RS_ERR_INVALID;
-  g_pass_skipping.store(on, std::memory_order_relaxed);
-  return RS_OK;
-}
-
-rs_status rs_set_small_sort(int on) {
-  if (on != 0 && on != 1) return RS_ERR_INVALID;
-  g_small_sort.store(on, std::memory_order_relaxed);
-  return RS_OK;
-}
-
-rs_status rs_set_tile_offsets(int precomputed) {
-  if (precomputed != 0 && precomputed != 1) return RS_ERR_INVALID;
-  g_tile_offsets.store(precomputed, std::memory_order_relaxed);
-  return RS_OK;
-}
-
-rs_status rs_set_lookback_timeout_ns(uint64_t ns) {
-  if (ns == 0) return RS_ERR_INVALID;
-  g_timeout_ns.store(ns, std::memory_order_relaxed);
-  return RS_OK;
-}
-
 rs_status rs_lookback_timeout_probe(uint32_t* word, uint64_t timeout_ns, void* stream,
                                     rs_status* result) {
-  if (!word || !result || timeout_ns == 0 || timeout_ns > 10000000000ull) return RS_ERR_INVALID;
+  if (!word || !result || timeout_ns == 0 || timeout_ns > kMaxTimeoutNs) return RS_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(word, 0, 8, s) != cudaSuccess) return RS_ERR_CUDA;
   cudaError_t e = timed_launch(4, 1, s, [&](int*) {
@@ -625,13 +673,14 @@ uint64_t rs_launch_count_reset(void) { return g_launches.exchange(0); }
 // ---------------------------------------------------------------------------
 // Key-value sort that allocates nothing.
 //
-// Some callers cannot allocate device memory at the point where they sort:
-// code that runs inside a stream capture, callers whose memory is owned by a
-// pool they may not grow, or plugins that are handed only the buffers they
-// work on.  For them the scratch of the sort lives in one fixed array in this
-// library's device image.  The array is created when the library's device
-// code is loaded and stays until the process exits, on every GPU that loads
-// the library, so it is kept small: sorts of at most kNoAllocMaxKeys keys.
+// Some callers cannot allocate device memory where they sort: callers whose
+// device memory is owned by a pool they may not grow, or plugins and
+// callbacks that are handed only the buffers they work on and have no
+// allocator of their own.  For them the scratch of the sort lives in one
+// fixed array in this library's device image.  The array is created when the
+// library's device code is loaded and stays until the process exits, on
+// every GPU that loads the library, so it is kept small: sorts of at most
+// kNoAllocMaxKeys keys.
 // ---------------------------------------------------------------------------
 namespace {
 constexpr size_t kNoAllocMaxKeys = size_t(1) << 18;     // 262,144 keys
@@ -642,6 +691,25 @@ void* g_noalloc_addr[kNoAllocMaxDevices] = {};
 }  // namespace
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+// The host-side name of the array is not a device address: its address on
+// the current device is looked up once per device, with that device current.
+rs_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return RS_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return RS_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr)
+      return RS_ERR_CUDA;
+    g_noalloc_addr[dev] = addr;
+  }
+  *out = g_noalloc_addr[dev];
+  return RS_OK;
+}
+}  // namespace
 
 extern "C" rs_status radix_sort_pairs_u32_noalloc(const uint32_t* keys_in, uint32_t* keys_out,
                                                   const uint32_t* vals_in, uint32_t* vals_out,
@@ -654,24 +722,23 @@ extern "C" rs_status radix_sort_pairs_u32_noalloc(const uint32_t* keys_in, uint3
   if (st != RS_OK) return st;
   if (p.total > kNoAllocScratchBytes) return RS_ERR_INVALID;
   if (n == 0) return RS_OK;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return RS_ERR_CUDA;
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return RS_ERR_INVALID;
   void* scratch = nullptr;
-  {
-    // The host-side name of the array is not a device address: look the
-    // address up once per device, with that device current.
-    std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (g_noalloc_addr[dev] == nullptr) {
-      void* addr = nullptr;
-      if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr)
-        return RS_ERR_CUDA;
-      g_noalloc_addr[dev] = addr;
-    }
-    scratch = g_noalloc_addr[dev];
-  }
+  st = noalloc_scratch(&scratch);
+  if (st != RS_OK) return st;
   // The sort's first kernel zeroes every part of the scratch that must start
   // at zero, so what an earlier call left there does not matter.
   return run_sort(p, keys_in, keys_out, vals_in, vals_out, KeyXform{0, 0}, scratch,
-                  kNoAllocScratchBytes, static_cast<cudaStream_t>(stream));
+                  kNoAllocScratchBytes, Options{}, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" rs_status radix_sort_pairs_u32_noalloc_status(void* stream) {
+  void* scratch = nullptr;
+  rs_status st = noalloc_scratch(&scratch);
+  if (st != RS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, scratch, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return RS_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RS_ERR_CUDA;
+  return word == kErrNone ? RS_OK : static_cast<rs_status>(word);
 }

@@ -11,13 +11,20 @@ namespace lsdrs {
 constexpr int kWarp = 32;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
-// Look-back status word: [P:1][A:1][value:30].  A = the tile's own digit
-// count is published; P = the inclusive prefix over the row's tiles up to
-// this one is published.  Zero means "nothing yet".
-constexpr uint32_t kFlagA = 1u << 30;
-constexpr uint32_t kFlagP = 1u << 31;
-constexpr uint32_t kValueMask = kFlagA - 1u;
-constexpr uint64_t kMaxRowLen = kValueMask;  // counts must fit in 30 bits
+// Look-back status word: [P:1][A:1][value] in 32 bits (30-bit value) or 64
+// bits (62-bit value).  A = the tile's own digit count is published; P = the
+// inclusive prefix over the row's tiles up to this one is published.  Zero
+// means "nothing yet".  Flag and value share one word, so one relaxed load
+// sees a consistent pair.
+template <class SW>
+struct LookbackWord {
+  static constexpr SW kFlagA = SW(1) << (8 * sizeof(SW) - 2);
+  static constexpr SW kFlagP = SW(1) << (8 * sizeof(SW) - 1);
+  static constexpr SW kValueMask = kFlagA - 1;
+};
+constexpr uint32_t kFlagA = LookbackWord<uint32_t>::kFlagA;
+constexpr uint32_t kFlagP = LookbackWord<uint32_t>::kFlagP;
+constexpr uint32_t kValueMask = LookbackWord<uint32_t>::kValueMask;
 
 // Device error word values (mirrors rs_status).
 constexpr uint32_t kErrNone = 0;
@@ -51,6 +58,17 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
 
 __device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// 64-bit look-back words (flat sorts of 2^30 keys or more).
+__device__ __forceinline__ uint64_t ld_relaxed(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
 // Streaming loads of data read exactly once per pass.
@@ -97,6 +115,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+
+// Limit on the second wait for a bulk copy whose first wait timed out: the
+// copy writes the CTA's shared memory, so the CTA waits for it (boundedly)
+// before going on.
+constexpr uint64_t kCopyDrainNs = 1000000000ull;
 
 // Wait for phase `parity` of `bar` to complete, giving up after timeout_ns.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,

@@ -23,7 +23,7 @@ __global__ void __launch_bounds__(kScanThreads * Q) digit_scan_kernel(ScanArgs a
   const int p = blockIdx.x % a.passes;
   const int nb = a.passes * a.radix;
 
-  uint32_t sum = 0;
+  uint32_t total = 0;
   if (d < a.radix) {
     const uint32_t* s = a.slots + row * a.chunks_per_row * static_cast<int64_t>(nb) +
                         p * a.radix + d;
@@ -33,21 +33,20 @@ __global__ void __launch_bounds__(kScanThreads * Q) digit_scan_kernel(ScanArgs a
       const uint32_t s1 = s[static_cast<int64_t>(c + Q) * nb];
       const uint32_t s2 = s[static_cast<int64_t>(c + 2 * Q) * nb];
       const uint32_t s3 = s[static_cast<int64_t>(c + 3 * Q) * nb];
-      sum += (s0 + s1) + (s2 + s3);
+      total += (s0 + s1) + (s2 + s3);
     }
-    for (; c < a.chunks_per_row; c += Q) sum += s[static_cast<int64_t>(c) * nb];
+    for (; c < a.chunks_per_row; c += Q) total += s[static_cast<int64_t>(c) * nb];
   }
   if (Q > 1) {
-    part[q][d] = sum;
+    part[q][d] = total;
     __syncthreads();
     if (q != 0) return;
-    sum = 0;
+    total = 0;
 #pragma unroll
-    for (int k = 0; k < Q; ++k) sum += part[k][d];
+    for (int k = 0; k < Q; ++k) total += part[k][d];
   }
   // block-wide exclusive scan of the totals over the first kScanThreads threads
   const int lane = d & 31, warp = d >> 5;
-  const uint32_t total = sum;
   uint32_t incl = total;
 #pragma unroll
   for (int o = 1; o < kWarp; o <<= 1) {
@@ -72,6 +71,7 @@ __global__ void __launch_bounds__(kScanThreads * Q) digit_scan_kernel(ScanArgs a
     const int64_t o = (row * a.passes + p) * a.radix + d;
     a.bases[o] = excl;
     if (a.hist_out) a.hist_out[o] = total;
+    if (a.bases_out) a.bases_out[o] = excl;
   }
 
   // Without pass skipping every pass runs.

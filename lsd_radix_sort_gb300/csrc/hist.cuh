@@ -158,9 +158,11 @@ __global__ void __launch_bounds__(kHistThreads, 1) upfront_hist_kernel(HistArgs 
   }
   __syncthreads();
 
-  const int64_t row = blockIdx.x / a.chunks_per_row;
-  const int chunk = blockIdx.x % a.chunks_per_row;
-  const int64_t begin = static_cast<int64_t>(chunk) * a.chunk_len;
+  // block -> (row, chunk of the row); 32-bit arithmetic (grids fit it)
+  const uint32_t row32 = blockIdx.x / static_cast<uint32_t>(a.chunks_per_row);
+  const int64_t row = row32;
+  const int64_t chunk = blockIdx.x - row32 * static_cast<uint32_t>(a.chunks_per_row);
+  const int64_t begin = chunk * a.chunk_len;
   const int64_t end = begin + a.chunk_len < a.cols ? begin + a.chunk_len : a.cols;
   const T* base = static_cast<const T*>(a.keys) + row * a.cols;
   uint32_t* col = cnt + (tid & (C - 1));
@@ -179,7 +181,7 @@ __global__ void __launch_bounds__(kHistThreads, 1) upfront_hist_kernel(HistArgs 
   }
   __syncthreads();
 
-  uint32_t* slot = a.slots + (row * a.chunks_per_row + chunk) * static_cast<int64_t>(nb);
+  uint32_t* slot = a.slots + static_cast<int64_t>(blockIdx.x) * nb;
   for (int b = tid; b < nb; b += kHistThreads) {
     uint32_t s = 0;
 #pragma unroll

@@ -68,7 +68,7 @@ struct SweepShape {
 #endif
 #ifndef LSDRS_F16_T
 #define LSDRS_F16_T 256
-#define LSDRS_F16_I 16
+#define LSDRS_F16_I 24
 #define LSDRS_F16_B 4
 #endif
 #ifndef LSDRS_F16_W
@@ -87,14 +87,18 @@ constexpr SweepShape sweep_shape(KeyKind k, ValKind v) {
 
 constexpr int kHistThreads = 1024;
 // K-HIST grid: one 1,024-thread CTA fits an SM (its counters take up to
-// 128 KB of shared memory), so a flat sort takes one wave, one CTA per SM
-// (152 SMs): no wave tail, and K-SCAN adds 152 partial counts per digit.
-#ifndef LSDRS_HIST_CTAS
-#define LSDRS_HIST_CTAS 152
-#endif
-constexpr int kHistTargetCtas = LSDRS_HIST_CTAS;
+// 128 KB of shared memory), so a flat sort takes one wave, one CTA per SM of
+// the device (device_sm_count): no wave tail.  Scratch is sized for at most
+// kMaxHistCtas chunks, which covers any current part.
+constexpr int kMaxHistCtas = 256;
 constexpr int64_t kHistMinChunk = 4096;
 constexpr int kScanThreads = 256;
+
+// Look-back words.  A 32-bit word holds [P:1][A:1][count:30], so it serves
+// every chain of fewer than 2^30 keys: every row of a row-wise sort and flat
+// sorts below 2^30 keys.  A flat sort of 2^30 keys or more uses 64-bit words,
+// [P:1][A:1][count:62].
+constexpr int64_t kMaxNarrowKeys = (int64_t(1) << 30) - 1;
 
 struct HistArgs {
   const void* keys;
@@ -147,7 +151,8 @@ struct ScanArgs {
   int passes;
   int radix;
   uint32_t* hist_out;      // optional [rows][passes][radix] totals
-  uint32_t* bases;         // [rows][passes][radix] exclusive scans
+  uint32_t* bases_out;     // optional [rows][passes][radix] exclusive scans
+  uint32_t* bases;         // [rows][passes][radix] exclusive scans (scratch)
   uint32_t* header;        // scratch header: nontrivial flags, schedule
   int in_place;            // the sort reads and writes the same buffer
   int dynamic;             // write the schedule codes into the tile counters
@@ -175,21 +180,25 @@ struct SweepArgs {
   int64_t full_per_row;    // tiles of a row that hold a whole tile of keys
   int shift;
   uint32_t mask;
+  uint32_t byte_sel;       // whole-byte digits: 0x4440 | byte index within a 32-bit word
+  int byte_hi;             //   and whether that word is the high half of a 64-bit key
   KeyXform xf;             // key transform
   const uint32_t* bases;   // bases of this pass for row 0
   int64_t bases_row_stride;
-  uint32_t* status_arr[2]; // look-back words [rows * full_per_row][radix], by parity
+  void* status_arr[2];     // look-back words [rows * full_per_row][radix], by parity
+                           // (u32, or u64 for flat sorts of 2^30 keys or more)
   uint32_t* tile_counter;  // (schedule code << kCodeShift, when dynamic) | tiles handed out:
                            // ids below rows * full_per_row are full tiles, then one
                            // partial tile per row when cols is not a whole number of tiles
+  int wide;                // 64-bit look-back words (flat sorts of 2^30 keys or more)
   int dynamic;             // the schedule comes from K-SCAN (pass skipping on)
   uint32_t code;           // otherwise: this pass's code, from the host, and
   const void* pass_keys_in;   // the buffers and look-back words it selects
   void* pass_keys_out;
   const void* pass_vals_in;
   void* pass_vals_out;
-  uint32_t* pass_status;
-  uint32_t* pass_status_zero;
+  void* pass_status;
+  void* pass_status_zero;
   const uint32_t* offsets; // [rows * tiles_per_row][radix] precomputed output offsets, or null
   uint32_t* error;
   uint64_t timeout_ns;
@@ -210,6 +219,15 @@ cudaError_t launch_sweep_x32(ValKind v, int bits, const SweepArgs& a, int* launc
 cudaError_t launch_sweep_x64(ValKind v, int bits, const SweepArgs& a, int* launched,
                              cudaStream_t s);
 cudaError_t launch_sweep_f16(const SweepArgs& a, int* launched, cudaStream_t s);
+// The same with 64-bit look-back words (flat sorts of 2^30 keys or more).
+cudaError_t launch_sweep_u32_wide(ValKind v, int bits, const SweepArgs& a, int* launched,
+                                  cudaStream_t s);
+cudaError_t launch_sweep_u64_wide(ValKind v, int bits, const SweepArgs& a, int* launched,
+                                  cudaStream_t s);
+cudaError_t launch_sweep_x32_wide(ValKind v, int bits, const SweepArgs& a, int* launched,
+                                  cudaStream_t s);
+cudaError_t launch_sweep_x64_wide(ValKind v, int bits, const SweepArgs& a, int* launched,
+                                  cudaStream_t s);
 
 // Precomputed tile offsets (row-wise sorts, instead of the look-back): per
 // pass, the digit counts of every tile of the pass's input, then per row and
@@ -263,6 +281,8 @@ struct FinishArgs {
   int64_t rows, cols;
 };
 cudaError_t launch_finish(const FinishArgs& f, cudaStream_t s);
+// Streaming multiprocessors of the current device (queried once per device).
+int device_sm_count();
 cudaError_t launch_timeout_probe(uint32_t* word, uint32_t* error, uint64_t timeout_ns,
                                  cudaStream_t s);
 

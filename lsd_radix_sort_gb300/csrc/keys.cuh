@@ -25,6 +25,11 @@
 
 namespace lsdrs {
 
+// digit_byte(k, sel, hi, xf): the digit when it is one whole byte of T(k)
+// (8-bit digits starting at a multiple of 8): byte (sel & 3) of the high
+// (hi) or low 32-bit word of T(k), by one byte permute; sel is
+// 0x4440 | byte index, so the upper three bytes of the result are zero.
+
 // Unsigned 32-bit keys in ascending order: T is the identity.
 struct KeyU32 {
   using T = uint32_t;
@@ -33,6 +38,10 @@ struct KeyU32 {
   __device__ __forceinline__ static uint32_t digit(T k, int shift, uint32_t mask,
                                                    const KeyXform&) {
     return (k >> shift) & mask;
+  }
+  __device__ __forceinline__ static uint32_t digit_byte(T k, uint32_t sel, bool,
+                                                        const KeyXform&) {
+    return __byte_perm(k, 0u, sel);
   }
 };
 
@@ -50,6 +59,10 @@ struct KeyX32 {
                                                         : static_cast<uint32_t>(x.pos));
     return (t >> shift) & mask;
   }
+  __device__ __forceinline__ static uint32_t digit_byte(T k, uint32_t sel, bool,
+                                                        const KeyXform& x) {
+    return __byte_perm(encode(k, x), 0u, sel);
+  }
 };
 
 struct KeyU64 {
@@ -59,6 +72,10 @@ struct KeyU64 {
   __device__ __forceinline__ static uint32_t digit(T k, int shift, uint32_t mask,
                                                    const KeyXform&) {
     return static_cast<uint32_t>(k >> shift) & mask;
+  }
+  __device__ __forceinline__ static uint32_t digit_byte(T k, uint32_t sel, bool hi,
+                                                        const KeyXform&) {
+    return __byte_perm(hi ? static_cast<uint32_t>(k >> 32) : static_cast<uint32_t>(k), 0u, sel);
   }
 };
 
@@ -72,6 +89,11 @@ struct KeyX64 {
                                                    const KeyXform& x) {
     const uint64_t t = k ^ (static_cast<int64_t>(k) < 0 ? x.neg : x.pos);
     return static_cast<uint32_t>(t >> shift) & mask;
+  }
+  __device__ __forceinline__ static uint32_t digit_byte(T k, uint32_t sel, bool hi,
+                                                        const KeyXform& x) {
+    const uint64_t t = encode(k, x);
+    return __byte_perm(hi ? static_cast<uint32_t>(t >> 32) : static_cast<uint32_t>(t), 0u, sel);
   }
 };
 
@@ -90,6 +112,10 @@ struct KeyF16Bits {
     const uint32_t t = u ^ ((u & 0x8000u) ? static_cast<uint32_t>(x.neg)
                                           : static_cast<uint32_t>(x.pos));
     return (t >> shift) & mask;
+  }
+  __device__ __forceinline__ static uint32_t digit_byte(T k, uint32_t sel, bool,
+                                                        const KeyXform& x) {
+    return __byte_perm(encode(k, x), 0u, sel);
   }
 };
 

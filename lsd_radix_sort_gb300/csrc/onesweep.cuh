@@ -47,6 +47,8 @@
 // of the tile, are not counted in the published counts and are not stored
 // (the page's sentinel padding, without the padding).
 #pragma once
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "keys.cuh"
@@ -65,6 +67,23 @@
 #endif
 #ifndef LSDRS_STATS
 #define LSDRS_STATS 0
+#endif
+// Where a tile runs its look-back: 0 after staging its keys and payloads,
+// 1 after the digit scan (before staging), 2 as soon as it has published
+// its own counts (the earliest point; successors then see inclusive prefixes
+// sooner and walk back fewer tiles).
+#ifndef LSDRS_LB_EARLY
+#define LSDRS_LB_EARLY 0
+#endif
+// Per-warp digit counters and offsets held in 16 bits (two per shared word)
+// instead of 32.
+#ifndef LSDRS_CNT16
+#define LSDRS_CNT16 1
+#endif
+// Whole-byte digits by one byte permute (8-bit digits starting at a multiple
+// of 8) instead of shift and mask.
+#ifndef LSDRS_BYTE_DIGITS
+#define LSDRS_BYTE_DIGITS 1
 #endif
 
 namespace lsdrs {
@@ -90,6 +109,16 @@ constexpr int kPhaseWord = 104;
   do {                 \
   } while (0)
 #endif
+
+// This pass's digit of key k: one byte permute when the digit is a whole
+// byte of the transformed key (BYTE), else shift and mask.
+template <class KeyOp, bool BYTE>
+__device__ __forceinline__ uint32_t pass_digit(typename KeyOp::T k, const SweepArgs& a) {
+  if constexpr (BYTE)
+    return KeyOp::digit_byte(k, a.byte_sel, a.byte_hi != 0, a.xf);
+  else
+    return KeyOp::digit(k, a.shift, a.mask, a.xf);
+}
 
 // Lanes of the warp whose digit equals this lane's digit.
 template <int BITS>
@@ -117,12 +146,13 @@ __device__ __forceinline__ uint32_t digit_peers(uint32_t d) {
 #endif
 }
 
-// Bounded wait for a non-zero look-back word.  On timeout, or when another
-// tile has already reported an error, records the error and returns a word
-// with flag P and value 0 so that the walk ends.
-__device__ __forceinline__ uint32_t wait_status(const uint32_t* p, uint32_t* error,
-                                                uint64_t timeout_ns, uint32_t& polls) {
-  uint32_t v = ld_relaxed(p);
+// Bounded wait for a non-zero look-back word (SW: uint32_t or uint64_t).
+// On timeout, or when another tile has already reported an error, records
+// the error and returns a word with flag P and value 0 so that the walk ends.
+template <class SW>
+__device__ __forceinline__ SW wait_status(const SW* p, uint32_t* error, uint64_t timeout_ns,
+                                          uint32_t& polls) {
+  SW v = ld_relaxed(p);
   if (v != 0) return v;
   const uint64_t t0 = global_timer_ns();
   uint32_t spins = 0;
@@ -135,12 +165,12 @@ __device__ __forceinline__ uint32_t wait_status(const uint32_t* p, uint32_t* err
     if (v != 0) break;
     if ((spins & 63u) == 0) {
       if (ld_relaxed(error) != kErrNone) {
-        v = kFlagP;
+        v = LookbackWord<SW>::kFlagP;
         break;
       }
       if (global_timer_ns() - t0 > timeout_ns) {
         atomicCAS(error, kErrNone, kErrLookback);
-        v = kFlagP;
+        v = LookbackWord<SW>::kFlagP;
         break;
       }
     }
@@ -155,24 +185,25 @@ __device__ __forceinline__ uint32_t wait_status(const uint32_t* p, uint32_t* err
 // of a warp these are coalesced 128-byte rows) and consumes them up to the
 // first inclusive prefix, or up to the first word not yet published, on
 // which it then waits.
-template <int R, int WIN>
-__device__ __forceinline__ uint32_t look_back(const uint32_t* col, int64_t t, uint32_t* error,
-                                              uint64_t timeout_ns, uint32_t& trips,
-                                              uint32_t& polls) {
+template <int R, int WIN, class SW>
+__device__ __forceinline__ SW look_back(const SW* col, int64_t t, uint32_t* error,
+                                        uint64_t timeout_ns, uint32_t& trips, uint32_t& polls) {
   static_assert(WIN >= 1 && WIN <= 32, "window of 1..32 tiles");
-  // Raw words are summed: the flag bits sit above bit 29 and the true sum
-  // of the counts stays below 2^30, so masking once at the end is exact.
-  uint32_t raw = 0;
+  using LW = LookbackWord<SW>;
+  // Raw words are summed: the flag bits sit above the value field and the
+  // true sum of the counts stays below its capacity (2^30 or 2^62), so
+  // masking once at the end is exact.
+  SW raw = 0;
   int pt = static_cast<int>(t) - 1;  // newest predecessor not yet consumed
   for (;;) {
-    const uint32_t* p = col + static_cast<int64_t>(pt) * R;  // word of tile pt
-    uint32_t v[WIN];
+    const SW* p = col + static_cast<int64_t>(pt) * R;  // word of tile pt
+    SW v[WIN];
     if (pt >= WIN - 1) {
 #pragma unroll
       for (int k = 0; k < WIN; ++k) v[k] = ld_relaxed(p - k * R);
     } else {
 #pragma unroll
-      for (int k = 0; k < WIN; ++k) v[k] = k <= pt ? ld_relaxed(p - k * R) : kFlagP;
+      for (int k = 0; k < WIN; ++k) v[k] = k <= pt ? ld_relaxed(p - k * R) : LW::kFlagP;
     }
     ++trips;
     // consume the window in order up to the first inclusive prefix (done),
@@ -182,12 +213,12 @@ __device__ __forceinline__ uint32_t look_back(const uint32_t* col, int64_t t, ui
     for (; k < WIN; ++k) {
       if (v[k] == 0) break;
       raw += v[k];
-      if (static_cast<int32_t>(v[k]) < 0) return raw & kValueMask;  // flag P
+      if (static_cast<std::make_signed_t<SW>>(v[k]) < 0) return raw & LW::kValueMask;  // flag P
     }
     if (k < WIN) {
-      const uint32_t w = wait_status(p - k * R, error, timeout_ns, polls);
+      const SW w = wait_status(p - k * R, error, timeout_ns, polls);
       raw += w;
-      if (w & kFlagP) return raw & kValueMask;
+      if (w & LW::kFlagP) return raw & LW::kValueMask;
       pt -= k + 1;
     } else {
       pt -= WIN;
@@ -196,12 +227,15 @@ __device__ __forceinline__ uint32_t look_back(const uint32_t* col, int64_t t, ui
 }
 
 // Shared-memory arrays every tile needs besides its key/payload buffers.
+// Per-warp counts and offsets stay below the tile size (< 2^16).
+using WarpCount = std::conditional_t<LSDRS_CNT16 != 0, uint16_t, uint32_t>;
 template <int W, int R>
 struct TileScratch {
-  alignas(16) uint32_t warp_cnt[W][R];  // per-warp digit counters, then per-warp offsets
+  alignas(16) WarpCount warp_cnt[W][R];  // per-warp digit counters, then per-warp offsets
   uint32_t warp_tot[W];     // per-warp sums of the digit-count scan
   uint32_t g_off[R];        // output position of staged slot j is g_off[d] + j
   uint32_t code;            // this pass's schedule code (kCode* bits)
+  uint32_t skip_stores;     // a copy into this tile's shared memory timed out
 };
 
 // This pass's buffers and look-back arrays, picked from the kernel
@@ -240,10 +274,10 @@ struct PassBufs {
     if (VK == kValIdx) return const_cast<void*>(last() ? a.vals[kBufOut] : a.vals[kBufAlt]);
     return const_cast<void*>(pick_buf(a.vals, dst()));
   }
-  __device__ __forceinline__ uint32_t* status() const {
+  __device__ __forceinline__ void* status() const {
     return DYN ? a.status_arr[(code & kCodeOdd) ? 1 : 0] : a.pass_status;
   }
-  __device__ __forceinline__ uint32_t* status_zero() const {
+  __device__ __forceinline__ void* status_zero() const {
     if (!DYN) return a.pass_status_zero;
     return last() ? nullptr : a.status_arr[(code & kCodeOdd) ? 0 : 1];
   }
@@ -262,14 +296,16 @@ struct TileIo {
 };
 
 // One tile: rank, publish, look back, stage, write.  Called by every thread
-// of the CTA; begins and ends with all threads converged.
+// of the CTA; begins and ends with all threads converged.  The tile is tile
+// t of its row; status_row points at the row's first look-back word (SW:
+// 32- or 64-bit words).
 template <bool FULL, bool DYN, bool PRE, class KeyOp, int BITS, int VK, int THREADS, int ITEMS,
-          int WIN>
+          int WIN, bool BYTE, class SW>
 __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
                                            TileScratch<THREADS / kWarp, (1 << BITS)>& s,
-                                           const TileIo<KeyOp>& io, uint32_t* status_row,
-                                           int64_t row, int64_t t, int64_t tile_begin,
-                                           int valid) {
+                                           const TileIo<KeyOp>& io, SW* status_row, int64_t row,
+                                           int64_t t, int64_t tile_begin, int valid) {
+  using LW = LookbackWord<SW>;
   using T = typename KeyOp::T;
   constexpr int R = 1 << BITS;
   constexpr int W = THREADS / kWarp;
@@ -281,7 +317,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const int64_t row_base = row * a.cols;
-  uint32_t* status_tile = status_row + t * R;
+  SW* status_tile = status_row + t * R;
   const int wpos = warp * WKEYS + lane;  // tile position of item 0
   uint32_t trips = 0, polls = 0;
 #if LSDRS_STATS >= 2
@@ -300,11 +336,11 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   // keep the tile's state in registers.
   constexpr int NP = (ITEMS + 1) / 2;
   uint32_t packed[NP];
-  uint32_t* wc = s.warp_cnt[warp];
+  WarpCount* wc = s.warp_cnt[warp];
   const uint32_t lt = lanemask_lt();
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
-    uint32_t d = KeyOp::digit(keys[i], a.shift, a.mask, a.xf);
+    uint32_t d = pass_digit<KeyOp, BYTE>(keys[i], a);
     if (!FULL && wpos + i * kWarp >= valid) d = R - 1;
     const uint32_t peers = digit_peers<BITS>(d);
     // Every peer lane reads the warp's count of its digit (one word per
@@ -312,7 +348,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     // count: the peers write the same value to the same word.
     const uint32_t before = wc[d];
     __syncwarp();
-    wc[d] = before + __popc(peers);
+    wc[d] = static_cast<WarpCount>(before + __popc(peers));
     __syncwarp();
     const uint32_t rank = before + __popc(peers & lt);
     if (i & 1)
@@ -331,19 +367,33 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   // thread d walks column d, so the column accesses are conflict-free).
   uint32_t my_count = 0;  // this tile's count of digit tid (without padding)
   uint32_t start = 0;     // first slot of digit tid in the tile
+  // ---- 6. decoupled look-back (thread d, digit d) ------------------------
+  // Sums the counts of the row's earlier tiles up to the first inclusive
+  // prefix and publishes this tile's inclusive prefix.  Run where
+  // LSDRS_LB_EARLY places it.  (PRE: the tile's output offsets were
+  // computed before the pass from per-tile digit counts: nothing to wait for.)
+  SW lb_excl = 0;
+  auto look_back_digit = [&]() {
+    if (!PRE && tid < R && t > 0) {
+      lb_excl = look_back<R, WIN>(status_row + tid, t, a.error, a.timeout_ns, trips, polls);
+      if (FULL) st_relaxed(status_tile + tid, LW::kFlagP | (lb_excl + my_count));
+    }
+  };
   {
     uint32_t total = 0;
     if (tid < R) {
 #pragma unroll
       for (int w = 0; w < W; ++w) {
         const uint32_t c = s.warp_cnt[w][tid];
-        s.warp_cnt[w][tid] = total;
+        s.warp_cnt[w][tid] = static_cast<WarpCount>(total);
         total += c;
       }
       my_count = (!FULL && tid == R - 1) ? total - static_cast<uint32_t>(TILE - valid) : total;
       // a partial tile is the last of its row: nothing waits on it
-      if (FULL && !PRE) st_relaxed(status_tile + tid, (t == 0 ? kFlagP : kFlagA) | my_count);
+      if (FULL && !PRE)
+        st_relaxed(status_tile + tid, (t == 0 ? LW::kFlagP : LW::kFlagA) | SW(my_count));
     }
+    if (LSDRS_LB_EARLY == 2) look_back_digit();
     uint32_t incl = total;
 #pragma unroll
     for (int o = 1; o < kWarp; o <<= 1) {
@@ -360,17 +410,19 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     start = before + incl - total;
     if (tid < R) {
 #pragma unroll
-      for (int w = 0; w < W; ++w) s.warp_cnt[w][tid] += start;
+      for (int w = 0; w < W; ++w)
+        s.warp_cnt[w][tid] = static_cast<WarpCount>(s.warp_cnt[w][tid] + start);
     }
   }
   __syncthreads();
   LSDRS_PHASE(2);  // digit scan
+  if (LSDRS_LB_EARLY == 1) look_back_digit();
 
   // ---- 5. stage keys, then payloads, in tile-sorted order ---------------
   auto half = [](uint32_t w, int i) -> uint32_t { return (i & 1) ? (w >> 16) : (w & 0xFFFFu); };
   auto item_digit = [&](int i) -> uint32_t {
     if (!FULL && wpos + i * kWarp >= valid) return R - 1;
-    return KeyOp::digit(keys[i], a.shift, a.mask, a.xf);
+    return pass_digit<KeyOp, BYTE>(keys[i], a);
   };
   // Two items at a time: their warp offsets are packed like their ranks,
   // so one add gives both staging slots (each below TILE < 2^16, so the low
@@ -387,10 +439,13 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   }
   if constexpr (kVals) {
     if (io.val_bar != nullptr && !mbar_wait_bounded(io.val_bar, 0, a.timeout_ns)) {
-      // the bulk copy did not land in time: report it, give it a second
-      // period to finish (it writes this CTA's shared memory), carry on
+      // The bulk copy did not land in time: report it and keep this tile's
+      // unverified payloads out of the output (its look-back still runs, so
+      // later tiles are released).  The copy writes this CTA's shared memory,
+      // so it gets a further bounded period to finish before the CTA moves on.
       atomicCAS(a.error, kErrNone, kErrLookback);
-      mbar_wait_bounded(io.val_bar, 0, a.timeout_ns);
+      s.skip_stores = 1;
+      mbar_wait_bounded(io.val_bar, 0, kCopyDrainNs);
     }
     // The payloads are staged in the buffer they were loaded into: read
     // every thread's payloads before any is overwritten.
@@ -407,18 +462,13 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   }
   LSDRS_PHASE(3);  // staging (thread 0's share)
 
-  // ---- 6. decoupled look-back -------------------------------------------
-  // (PRE: the tile's output offsets were computed before the pass from
-  // per-tile digit counts, so there is nothing to wait for)
+  // ---- output offset of each digit's run ---------------------------------
+  if (LSDRS_LB_EARLY == 0) look_back_digit();
   if (PRE && tid < R) {
     s.g_off[tid] = a.offsets[(row * a.tiles_per_row + t) * R + tid] - start;
   } else if (tid < R) {
-    uint32_t excl = 0;
-    if (t > 0) {
-      excl = look_back<R, WIN>(status_row + tid, t, a.error, a.timeout_ns, trips, polls);
-      if (FULL) st_relaxed(status_tile + tid, kFlagP | (excl + my_count));
-    }
-    s.g_off[tid] = a.bases[row * a.bases_row_stride + tid] + excl - start;
+    // output positions are below 2^32 (flat sorts) or 2^30 (rows)
+    s.g_off[tid] = a.bases[row * a.bases_row_stride + tid] + static_cast<uint32_t>(lb_excl) - start;
   }
   LSDRS_PHASE(4);  // thread 0's look-back
 #if LSDRS_STATS
@@ -427,6 +477,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
 #endif
   __syncthreads();
   LSDRS_PHASE(5);  // wait for the slowest digit's look-back
+  if (s.skip_stores) return;  // (uniform: read after the barrier)
 
   // ---- 7. contiguous per-digit runs out ---------------------------------
   const PassBufs<DYN> pb{DYN ? s.code : a.code, a};
@@ -441,7 +492,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
       const T k = io.stage_keys[j];
       uint32_t v = 0;
       if constexpr (kVals) v = io.vals[j];
-      const uint32_t d = KeyOp::digit(k, a.shift, a.mask, a.xf);
+      const uint32_t d = pass_digit<KeyOp, BYTE>(k, a);
       const uint32_t g = s.g_off[d] + static_cast<uint32_t>(j);
       kout[g] = k;
       if constexpr (kVals) {
@@ -475,9 +526,11 @@ struct SweepSmem {
 // DYN: the schedule (which passes run, between which buffers) comes from
 // K-SCAN through the tile counter; otherwise it is the host's static one in
 // the kernel arguments (every pass runs).
-template <bool DYN, bool PRE, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN>
+template <bool DYN, bool PRE, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int WIN,
+          bool BYTE, bool WIDE>
 __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
   using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
+  using SW = std::conditional_t<WIDE, uint64_t, uint32_t>;  // look-back word
   using T = typename KeyOp::T;
   constexpr int R = 1 << BITS;
   constexpr int W = THREADS / kWarp;
@@ -495,9 +548,11 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
     s.tile_id = v & kTileMask;
     if (DYN) s.scratch.code = v >> kCodeShift;
     s.abort = ld_relaxed(a.error) != kErrNone;
+    s.scratch.skip_stores = 0;
   }
-  static_assert((W * R) % 4 == 0, "counters are zeroed 16 bytes at a time");
-  for (int i = tid; i < W * R / 4; i += THREADS)
+  constexpr int kCnt16B = W * R * static_cast<int>(sizeof(WarpCount)) / 16;
+  static_assert((W * R * sizeof(WarpCount)) % 16 == 0, "counters are zeroed 16 bytes at a time");
+  for (int i = tid; i < kCnt16B; i += THREADS)
     reinterpret_cast<uint4*>(&s.scratch.warp_cnt[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
 
@@ -510,7 +565,7 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
     t = a.full_per_row;
     tile_begin = t * TILE;
   } else {
-    // tile ids and tiles per row fit 32 bits (at most 2^30 keys)
+    // tile ids are below 2^24, so 32-bit arithmetic suffices
     const uint32_t id = s.tile_id;
     const uint32_t r32 = id / fpr;
     row = r32;
@@ -523,7 +578,7 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
   const PassBufs<DYN> pb{DYN ? s.scratch.code : a.code, a};
   // look-back words are indexed by full tile, row-major: row r's tile t at
   // r * full_per_row + t; partial tiles publish none
-  uint32_t* status_row = pb.status() + (row * a.full_per_row) * R;
+  SW* status_row = static_cast<SW*>(pb.status()) + (row * a.full_per_row) * R;
   TileIo<KeyOp> io;
   io.key_src = static_cast<const T*>(pb.keys_in()) + off;
   io.stage_keys = s.stage;
@@ -531,7 +586,7 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
   io.val_bar = nullptr;
   io.vals_in = false;
   if (s.abort) {  // an earlier tile failed: release successors and stop
-    if (full && !PRE && tid < R) st_relaxed(status_row + t * R + tid, kFlagP);
+    if (full && !PRE && tid < R) st_relaxed(status_row + t * R + tid, LookbackWord<SW>::kFlagP);
   } else {
     if (VK != kValNone && pb.template vals_in<VK>() != nullptr) {
       // Payloads are not needed before the staging step: a full tile with an
@@ -553,24 +608,22 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
       }
     }
     if (!full) {
-      sweep_tile<false, DYN, PRE, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io,
-                                                                       status_row, row, t,
-                                                                       tile_begin, valid);
+      sweep_tile<false, DYN, PRE, KeyOp, BITS, VK, THREADS, ITEMS, WIN, BYTE>(
+          a, s.scratch, io, status_row, row, t, tile_begin, valid);
     } else {
-      sweep_tile<true, DYN, PRE, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a, s.scratch, io,
-                                                                      status_row, row, t,
-                                                                      tile_begin, valid);
+      sweep_tile<true, DYN, PRE, KeyOp, BITS, VK, THREADS, ITEMS, WIN, BYTE>(
+          a, s.scratch, io, status_row, row, t, tile_begin, valid);
     }
   }
-  uint32_t* zero = PassBufs<DYN>{DYN ? s.scratch.code : a.code, a}.status_zero();
+  SW* zero = static_cast<SW*>(PassBufs<DYN>{DYN ? s.scratch.code : a.code, a}.status_zero());
   if (full && !PRE && zero != nullptr && tid < R)
     zero[static_cast<int64_t>(s.tile_id) * R + tid] = 0;
 }
 
 template <bool DYN, bool PRE, class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB,
-          int WIN>
+          int WIN, bool BYTE, bool WIDE>
 __global__ void __launch_bounds__(THREADS, MINB) onesweep_kernel(SweepArgs a) {
-  onesweep_body<DYN, PRE, KeyOp, BITS, VK, THREADS, ITEMS, WIN>(a);
+  onesweep_body<DYN, PRE, KeyOp, BITS, VK, THREADS, ITEMS, WIN, BYTE, WIDE>(a);
 }
 
 template <class K>
@@ -588,40 +641,52 @@ cudaError_t launch_with_smem(K kern, unsigned grid, int threads, size_t smem, cu
 // One pass: every full tile, then each row's partial tile, in one launch.
 // Returns the number of kernels launched in *launched.
 // PRE: offsets precomputed by the tile-count kernels (row-wise sorts only).
+// WIDE: 64-bit look-back words (flat sorts of 2^30 keys or more).
 template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS, int MINB, int WIN,
-          bool PRE = false>
+          bool PRE = false, bool WIDE = false>
 cudaError_t launch_sweep_t(const SweepArgs& args, int* launched, cudaStream_t s) {
   using S = SweepSmem<KeyOp, BITS, VK, THREADS, ITEMS>;
   constexpr int TILE = S::kTile;
-  SweepArgs a = args;
+  const SweepArgs& a = args;
   *launched = 0;
   const int64_t full = a.rows * a.full_per_row;
   const bool partial = a.rows > 0 && a.cols % TILE != 0;
   const int64_t grid = full + (partial ? a.rows : 0);
-  if (grid > 0) {
-    cudaError_t e =
-        a.dynamic
-            ? launch_with_smem(onesweep_kernel<true, PRE, KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>,
-                               static_cast<unsigned>(grid), THREADS, sizeof(S), s, a)
-            : launch_with_smem(onesweep_kernel<false, PRE, KeyOp, BITS, VK, THREADS, ITEMS, MINB, WIN>,
-                               static_cast<unsigned>(grid), THREADS, sizeof(S), s, a);
-    if (e != cudaSuccess) return e;
-    ++*launched;
-  }
+  if (grid <= 0) return cudaSuccess;
+  // whole-byte digits (every 8-bit pass but a narrower last one) take the
+  // byte-permute instantiation
+  const bool byte = LSDRS_BYTE_DIGITS && BITS == 8 && a.shift % 8 == 0 && a.mask == 0xFFu;
+  const unsigned g = static_cast<unsigned>(grid);
+  constexpr bool B8 = LSDRS_BYTE_DIGITS && BITS == 8;
+  cudaError_t e;
+  if (byte)
+    e = a.dynamic
+            ? launch_with_smem(onesweep_kernel<true, PRE, KeyOp, BITS, VK, THREADS, ITEMS, MINB,
+                                               WIN, B8, WIDE>, g, THREADS, sizeof(S), s, a)
+            : launch_with_smem(onesweep_kernel<false, PRE, KeyOp, BITS, VK, THREADS, ITEMS, MINB,
+                                               WIN, B8, WIDE>, g, THREADS, sizeof(S), s, a);
+  else
+    e = a.dynamic
+            ? launch_with_smem(onesweep_kernel<true, PRE, KeyOp, BITS, VK, THREADS, ITEMS, MINB,
+                                               WIN, false, WIDE>, g, THREADS, sizeof(S), s, a)
+            : launch_with_smem(onesweep_kernel<false, PRE, KeyOp, BITS, VK, THREADS, ITEMS, MINB,
+                                               WIN, false, WIDE>, g, THREADS, sizeof(S), s, a);
+  if (e != cudaSuccess) return e;
+  *launched = 1;
   return cudaSuccess;
 }
 
-template <class KeyOp, int VK, int THREADS, int ITEMS, int MINB, int WIN>
+template <class KeyOp, int VK, int THREADS, int ITEMS, int MINB, int WIN, bool WIDE = false>
 cudaError_t launch_sweep_bits(int bits, const SweepArgs& a, int* launched, cudaStream_t s) {
   switch (bits) {
-    case 1: return launch_sweep_t<KeyOp, 1, VK, THREADS, ITEMS, MINB, WIN>(a, launched, s);
-    case 2: return launch_sweep_t<KeyOp, 2, VK, THREADS, ITEMS, MINB, WIN>(a, launched, s);
-    case 3: return launch_sweep_t<KeyOp, 3, VK, THREADS, ITEMS, MINB, WIN>(a, launched, s);
-    case 4: return launch_sweep_t<KeyOp, 4, VK, THREADS, ITEMS, MINB, WIN>(a, launched, s);
-    case 5: return launch_sweep_t<KeyOp, 5, VK, THREADS, ITEMS, MINB, WIN>(a, launched, s);
-    case 6: return launch_sweep_t<KeyOp, 6, VK, THREADS, ITEMS, MINB, WIN>(a, launched, s);
-    case 7: return launch_sweep_t<KeyOp, 7, VK, THREADS, ITEMS, MINB, WIN>(a, launched, s);
-    case 8: return launch_sweep_t<KeyOp, 8, VK, THREADS, ITEMS, MINB, WIN>(a, launched, s);
+    case 1: return launch_sweep_t<KeyOp, 1, VK, THREADS, ITEMS, MINB, WIN, false, WIDE>(a, launched, s);
+    case 2: return launch_sweep_t<KeyOp, 2, VK, THREADS, ITEMS, MINB, WIN, false, WIDE>(a, launched, s);
+    case 3: return launch_sweep_t<KeyOp, 3, VK, THREADS, ITEMS, MINB, WIN, false, WIDE>(a, launched, s);
+    case 4: return launch_sweep_t<KeyOp, 4, VK, THREADS, ITEMS, MINB, WIN, false, WIDE>(a, launched, s);
+    case 5: return launch_sweep_t<KeyOp, 5, VK, THREADS, ITEMS, MINB, WIN, false, WIDE>(a, launched, s);
+    case 6: return launch_sweep_t<KeyOp, 6, VK, THREADS, ITEMS, MINB, WIN, false, WIDE>(a, launched, s);
+    case 7: return launch_sweep_t<KeyOp, 7, VK, THREADS, ITEMS, MINB, WIN, false, WIDE>(a, launched, s);
+    case 8: return launch_sweep_t<KeyOp, 8, VK, THREADS, ITEMS, MINB, WIN, false, WIDE>(a, launched, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,5 +1,7 @@
 // Measurement and failure-detection kernels: the copy roofline probe and a
 // look-back wait on a word that nothing sets.
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -48,12 +50,24 @@ __global__ void timeout_probe_kernel(uint32_t* word, uint32_t* error, uint64_t t
 
 }  // namespace
 
+int device_sm_count() {
+  constexpr int kMaxDevices = 64;
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+  if (dev < kMaxDevices) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+    return 1;
+  if (dev < kMaxDevices) cache[dev].store(sms, std::memory_order_relaxed);
+  return sms;
+}
+
 cudaError_t launch_copy(void* dst, const void* src, size_t bytes, cudaStream_t s) {
-  int dev = 0, sms = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e != cudaSuccess) return e;
+  const int sms = device_sm_count();
   const size_t n16 = bytes / 16;
   size_t want = (n16 + kCopyThreads * 4 - 1) / (kCopyThreads * 4);
   size_t grid = static_cast<size_t>(sms) * 4;
@@ -113,7 +127,8 @@ cudaError_t launch_finish(const FinishArgs& f, cudaStream_t s) {
   if (f.keys_bytes % 2 || f.vals_bytes % 2) return cudaErrorInvalidValue;
   const size_t units = (f.keys_bytes > f.vals_bytes ? f.keys_bytes : f.vals_bytes) / 16;
   size_t grid = (units + kCopyThreads - 1) / kCopyThreads;
-  if (grid > 4 * 152) grid = 4 * 152;
+  const size_t cap = 4 * static_cast<size_t>(device_sm_count());
+  if (grid > cap) grid = cap;
   if (grid == 0) grid = 1;
   finish_kernel<<<static_cast<unsigned>(grid), kCopyThreads, 0, s>>>(f);
   return cudaGetLastError();

@@ -46,16 +46,22 @@ def test_status_strings(lib):
 
 def test_temp_bytes_query(lib):
     out = ctypes.c_size_t(0)
-    assert lib.radix_sort_temp_bytes(1 << 20, 4, 4, 0, 32, 8, ctypes.byref(out)) == 0
+    assert lib.radix_sort_keys_temp_bytes(1 << 20, 4, 4, 0, 32, 8, ctypes.byref(out)) == 0
     n = 1 << 20
     assert out.value >= n * 8            # alternate keys + payloads
     small = ctypes.c_size_t(0)
-    assert lib.radix_sort_temp_bytes(1 << 20, 4, 0, 0, 32, 8, ctypes.byref(small)) == 0
+    assert lib.radix_sort_keys_temp_bytes(1 << 20, 4, 0, 0, 32, 8, ctypes.byref(small)) == 0
     assert small.value < out.value
     assert lib.radix_segmented_sort_temp_bytes(1024, 65536, ctypes.byref(out)) == 0
     assert lib.radix_segmented_sort_temp_bytes(1 << 40, 1 << 10, ctypes.byref(out)) == 1
     assert out.value >= 1024 * 65536 * 6  # alternate keys + int32 indices
-    assert lib.radix_sort_temp_bytes(0, 4, 0, 0, 32, 8, ctypes.byref(out)) == 0
+    assert lib.radix_sort_keys_temp_bytes(0, 4, 0, 0, 32, 8, ctypes.byref(out)) == 0
+    # flat sorts of 2^30 keys and more are accepted (segmented look-back), up
+    # to 2^32 - 1; a row of a row-wise sort stays below 2^30
+    assert lib.radix_sort_keys_temp_bytes((1 << 32) - 1, 4, 4, 0, 32, 8, ctypes.byref(out)) == 0
+    assert out.value >= ((1 << 32) - 1) * 8
+    assert lib.radix_segmented_sort_temp_bytes(1, 1 << 30, ctypes.byref(out)) == 1
+    assert lib.radix_segmented_sort_temp_bytes(2, (1 << 30) - 1, ctypes.byref(out)) == 0
 
 
 @pytest.mark.parametrize("args", [
@@ -66,11 +72,11 @@ def test_temp_bytes_query(lib):
     (1 << 10, 4, 0, -1, 8, 8),
     (1 << 10, 4, 0, 0, 32, 0),       # digit width
     (1 << 10, 4, 0, 0, 32, 9),
-    (1 << 30, 4, 0, 0, 32, 8),       # beyond RS_MAX_KEYS
+    (1 << 32, 4, 0, 0, 32, 8),       # beyond RS_MAX_KEYS
 ])
 def test_temp_bytes_rejects(lib, args):
     out = ctypes.c_size_t(0)
-    assert lib.radix_sort_temp_bytes(*args, ctypes.byref(out)) == 1
+    assert lib.radix_sort_keys_temp_bytes(*args, ctypes.byref(out)) == 1
 
 
 def test_sort_calls_validate_before_launch(lib):
@@ -83,7 +89,7 @@ def test_sort_calls_validate_before_launch(lib):
     assert lib.radix_sort_keys_u64(bogus, bogus, 100, 0, 65, 8, temp, big, None) == 1
     assert lib.radix_sort_pairs_u32(bogus, bogus, bogus, bogus, 100, 5, 5, 8, temp, big, None) == 1
     # too many keys
-    assert lib.radix_sort_keys_u32(bogus, bogus, 1 << 30, 0, 32, 8, temp, big, None) == 1
+    assert lib.radix_sort_keys_u32(bogus, bogus, 1 << 32, 0, 32, 8, temp, big, None) == 1
     # temp too small
     assert lib.radix_sort_keys_u32(bogus, ctypes.c_void_p(0x90000000), 100, 0, 32, 8, temp, 16,
                                    None) == 2
@@ -110,26 +116,57 @@ def test_sort_calls_validate_before_launch(lib):
     assert lib.radix_segmented_sort_f16(bogus, bogus, bogus, 1 << 62, 4, 0, 0, temp, big,
                                         None) == 1
     # typed sorts: unknown key type, bad descending flag, bad bit range, n == 0
-    assert lib.radix_sort_keys_typed(9, 0, bogus, bogus, 100, 0, 32, 8, temp, big, None) == 1
-    assert lib.radix_sort_keys_typed(-1, 0, bogus, bogus, 100, 0, 32, 8, temp, big, None) == 1
-    assert lib.radix_sort_keys_typed(1, 2, bogus, bogus, 100, 0, 32, 8, temp, big, None) == 1
-    assert lib.radix_sort_keys_typed(2, 0, bogus, bogus, 100, 0, 33, 8, temp, big, None) == 1
+    assert lib.radix_sort_keys_typed(9, 0, bogus, bogus, 100, 0, 32, 8, temp, big, None,
+                                     None) == 1
+    assert lib.radix_sort_keys_typed(-1, 0, bogus, bogus, 100, 0, 32, 8, temp, big, None,
+                                     None) == 1
+    assert lib.radix_sort_keys_typed(1, 2, bogus, bogus, 100, 0, 32, 8, temp, big, None,
+                                     None) == 1
+    assert lib.radix_sort_keys_typed(2, 0, bogus, bogus, 100, 0, 33, 8, temp, big, None,
+                                     None) == 1
     assert lib.radix_sort_pairs_typed(5, 1, bogus, bogus, bogus, bogus, 100, 0, 65, 8, temp, big,
-                                      None) == 1
+                                      None, None) == 1
     assert lib.radix_sort_pairs_typed(4, 0, bogus, bogus, None, None, 100, 0, 64, 8, temp, big,
-                                      None) == 1
-    assert lib.radix_sort_keys_typed(2, 1, None, None, 0, 0, 32, 8, None, 0, None) == 0
+                                      None, None) == 1
+    assert lib.radix_sort_keys_typed(2, 1, None, None, 0, 0, 32, 8, None, 0, None, None) == 0
     # histograms: bad key width
     assert lib.radix_sort_histograms(bogus, 2, 100, 0, 16, 8, bogus, bogus, temp, big, None) == 1
     # copy probe: misaligned sizes
     assert lib.rs_copy_probe(bogus, temp, 15, None) == 1
-    assert lib.rs_set_lookback_timeout_ns(0) == 1
-    assert lib.rs_set_lookback_timeout_ns(2_000_000_000) == 0
-    # process-wide switches take 0 or 1 (restored to their defaults)
-    for name, default in (("rs_set_pass_skipping", 0), ("rs_set_tile_offsets", 0),
-                          ("rs_set_small_sort", 1)):
-        assert getattr(lib, name)(2) == 1 and getattr(lib, name)(-1) == 1
-        assert getattr(lib, name)(1 - default) == 0 and getattr(lib, name)(default) == 0
+    # look-back probe: wait limit above 60 s
+    assert lib.rs_lookback_timeout_probe(bogus, 61_000_000_000, None, ctypes.byref(
+        ctypes.c_int(0))) == 1
+
+
+def test_options_validated_before_launch(lib):
+    """Per-call options: unknown flag bits and a wait limit above 60 s are
+    refused on the host; the pointers are never touched."""
+    import lsd_radix_sort_gb300 as rs
+    bogus = ctypes.c_void_p(0x1000)
+    out = ctypes.c_void_p(0x90000000)
+    temp = ctypes.c_void_p(0x100000)
+    big = 1 << 40
+    n = 100_000
+    for opts in (rs.Options(0x8, 0), rs.Options(0, 61_000_000_000)):
+        assert lib.radix_sort_pairs_typed(0, 0, bogus, out, ctypes.c_void_p(0x50000000),
+                                          ctypes.c_void_p(0x60000000), n, 0, 32, 8, temp, big,
+                                          ctypes.byref(opts), None) == 1
+    assert lib.radix_sort_keys_typed(1, 0, bogus, out, n, 0, 32, 8, temp, big,
+                                     ctypes.byref(rs.Options(0x10, 0)), None) == 1
+    assert lib.radix_segmented_sort_f16_ex(bogus, out, ctypes.c_void_p(0x50000000), 2, 100, 0, 0,
+                                           temp, big, ctypes.byref(rs.Options(0x80, 0)),
+                                           None) == 1
+
+
+def test_temp_bytes_widen_lookback_words_from_2p30(lib):
+    """From 2^30 keys a flat sort's look-back words are 64-bit: the scratch
+    grows by the status arrays' second half, beyond the ping-pong buffers."""
+    a, b = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    n = (1 << 30) - 1
+    assert lib.radix_sort_keys_temp_bytes(n, 4, 4, 0, 32, 8, ctypes.byref(a)) == 0
+    assert lib.radix_sort_keys_temp_bytes(n + 1, 4, 4, 0, 32, 8, ctypes.byref(b)) == 0
+    tiles = -(-(n + 1) // 5888)
+    assert b.value - a.value >= 2 * tiles * 256 * 4  # two status arrays, 4 more bytes a word
 
 
 def test_product_path_fails_loudly_without_library(monkeypatch, tmp_path):

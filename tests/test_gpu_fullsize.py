@@ -62,3 +62,75 @@ def test_u64_pairs_2p28(rs, dist, begin, end):
     assert rs.device_status(temp) == rs.RS_OK
     del dk, dv
     check_sorted_pairs(keys, to_host(vo, np.uint32), to_host(ko, np.uint64), begin, end)
+
+
+def test_u32_pairs_above_2p30(rs):
+    """2^30 + 12,345 keys: past the 30-bit count of a 32-bit look-back word, so
+    the look-back runs on 64-bit words.  Checked on the device by the same
+    properties, plus sampled closed-form ranks."""
+    n = (1 << 30) + 12345
+    keys = workloads.u32_uniform(n, 1)
+    dk = to_dev(keys)
+    dv = to_dev(workloads.index_payload(n))
+    del keys
+    temp = torch.empty(rs.temp_bytes(n, 4, 4, 0, 32, 8), dtype=torch.uint8, device="cuda")
+    ko, vo = rs.radix_sort_pairs(dk, dv, temp=temp)
+    assert rs.device_status(temp) == rs.RS_OK
+    del temp, dv
+    flip = torch.tensor(-(1 << 31), dtype=torch.int32, device="cuda")
+    ks = ko ^ flip  # unsigned order as signed order
+    assert bool((ks[1:] >= ks[:-1]).all()), "keys decrease"
+    ties = ks[1:] == ks[:-1]
+    assert bool((vo[1:][ties] > vo[:-1][ties]).all()), "ties out of input order"
+    del ks, ties
+    idx = vo.long()  # payloads are input positions below 2^31
+    assert torch.equal(dk[idx], ko), "keys do not follow their payloads"
+    seen = torch.zeros(n, dtype=torch.bool, device="cuda")
+    seen[idx] = True
+    assert bool(seen.all()), "payloads are not a permutation"
+    del seen, idx
+    dks = dk ^ flip
+    rng = np.random.default_rng(3)
+    for i in [0, n - 1, *rng.integers(0, n, 4).tolist()]:
+        k = dks[i]
+        pos = int((dks < k).sum()) + int((dks[:i] == k).sum())
+        assert int(vo[pos]) == i and int(ko[pos]) == int(dk[i]), f"sampled rank of input {i}"
+
+
+def _const_byte_keys(n, seed):
+    # bits 8..15 constant: with pass skipping three of four passes run
+    return (workloads.u32_uniform(n, seed) & np.uint32(0xFFFF00FF)) | np.uint32(0x5A00)
+
+
+@pytest.mark.parametrize("case", ["keys_only", "pairs_pass_skipping"])
+def test_u32_above_2p30_keys_and_skipping(rs, case):
+    """The 64-bit look-back words with keys only (checked against the sorted
+    multiset), and with pass skipping (the device-side schedule) checked by
+    the properties above."""
+    n = (1 << 30) + 777
+    flip = torch.tensor(-(1 << 31), dtype=torch.int32, device="cuda")
+    if case == "keys_only":
+        dk = to_dev(workloads.u32_uniform(n, 2))
+        temp = torch.empty(rs.temp_bytes(n, 4, 0, 0, 32, 8), dtype=torch.uint8, device="cuda")
+        ko = rs.radix_sort_keys(dk, temp=temp)
+        assert rs.device_status(temp) == rs.RS_OK
+        del temp
+        want = torch.sort(dk ^ flip).values
+        assert torch.equal(ko ^ flip, want)
+        return
+    dk = to_dev(_const_byte_keys(n, 3))
+    dv = to_dev(workloads.index_payload(n))
+    temp = torch.empty(rs.temp_bytes(n, 4, 4, 0, 32, 8), dtype=torch.uint8, device="cuda")
+    ko, vo = rs.radix_sort_pairs(dk, dv, temp=temp, pass_skipping=True)
+    assert rs.device_status(temp) == rs.RS_OK and rs.passes_run(temp) == 3
+    del temp, dv
+    ks = ko ^ flip
+    assert bool((ks[1:] >= ks[:-1]).all()), "keys decrease"
+    ties = ks[1:] == ks[:-1]
+    assert bool((vo[1:][ties] > vo[:-1][ties]).all()), "ties out of input order"
+    del ks, ties
+    idx = vo.long()
+    assert torch.equal(dk[idx], ko), "keys do not follow their payloads"
+    seen = torch.zeros(n, dtype=torch.bool, device="cuda")
+    seen[idx] = True
+    assert bool(seen.all()), "payloads are not a permutation"

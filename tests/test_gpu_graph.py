@@ -28,26 +28,23 @@ def capture(fn):
 @pytest.mark.parametrize("n", [1000, 70_001])
 @pytest.mark.parametrize("skipping", [False, True])
 def test_graph_replay_sorts_new_inputs(rs, n, skipping):
-    rs.set_pass_skipping(skipping)
-    try:
-        dk = torch.empty(n, dtype=torch.int32, device="cuda")
-        dv = torch.empty(n, dtype=torch.int32, device="cuda")
-        ko, vo = torch.empty_like(dk), torch.empty_like(dv)
-        temp = torch.empty(rs.temp_bytes(n, 4, 4, 0, 32, 8), dtype=torch.uint8, device="cuda")
-        dk.copy_(torch.from_numpy(workloads.u32_uniform(n, 0).view(np.int32)))
-        dv.copy_(torch.from_numpy(workloads.index_payload(n).view(np.int32)))
-        g = capture(lambda: rs.radix_sort_pairs(dk, dv, ko, vo, 0, 32, 8, temp=temp))
-        for seed, dist in ((1, "uniform"), (2, "low_entropy"), (3, "all_equal"), (4, "sorted")):
-            keys = workloads.U32_DISTRIBUTIONS[dist](n, seed)
-            vals = workloads.index_payload(n)
-            dk.copy_(torch.from_numpy(keys.view(np.int32)))
-            g.replay()
-            torch.cuda.synchronize()
-            ek, ev = oracle.sort(keys, vals, 0, 32, 8)
-            assert np.array_equal(ko.cpu().numpy().view(np.uint32), ek), dist
-            assert np.array_equal(vo.cpu().numpy().view(np.uint32), ev), dist
-    finally:
-        rs.set_pass_skipping(False)
+    dk = torch.empty(n, dtype=torch.int32, device="cuda")
+    dv = torch.empty(n, dtype=torch.int32, device="cuda")
+    ko, vo = torch.empty_like(dk), torch.empty_like(dv)
+    temp = torch.empty(rs.temp_bytes(n, 4, 4, 0, 32, 8), dtype=torch.uint8, device="cuda")
+    dk.copy_(torch.from_numpy(workloads.u32_uniform(n, 0).view(np.int32)))
+    dv.copy_(torch.from_numpy(workloads.index_payload(n).view(np.int32)))
+    g = capture(lambda: rs.radix_sort_pairs(dk, dv, ko, vo, 0, 32, 8, temp=temp,
+                                            pass_skipping=skipping))
+    for seed, dist in ((1, "uniform"), (2, "low_entropy"), (3, "all_equal"), (4, "sorted")):
+        keys = workloads.U32_DISTRIBUTIONS[dist](n, seed)
+        vals = workloads.index_payload(n)
+        dk.copy_(torch.from_numpy(keys.view(np.int32)))
+        g.replay()
+        torch.cuda.synchronize()
+        ek, ev = oracle.sort(keys, vals, 0, 32, 8)
+        assert np.array_equal(ko.cpu().numpy().view(np.uint32), ek), dist
+        assert np.array_equal(vo.cpu().numpy().view(np.uint32), ev), dist
 
 
 def test_graph_replay_rows(rs):

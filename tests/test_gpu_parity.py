@@ -13,22 +13,22 @@ pytestmark = pytest.mark.gpu
 
 # tile sizes of the sweep kernels (keys per CTA), so that ragged cases
 # straddle tile boundaries
-TILE_U32_KEYS, TILE_U32_PAIRS, TILE_U64, TILE_U64_PAIRS, TILE_F16 = 7168, 5888, 4096, 4608, 4096
+TILE_U32_KEYS, TILE_U32_PAIRS, TILE_U64, TILE_U64_PAIRS, TILE_F16 = 7168, 5888, 4096, 4608, 6144
 
 
-def run_keys(rs, keys, begin=0, end=None, bits=8):
+def run_keys(rs, keys, begin=0, end=None, bits=8, **opts):
     d = to_dev(keys)
     out = poisoned_like(d)
-    rs.radix_sort_keys(d, out, begin, end, bits)
+    rs.radix_sort_keys(d, out, begin, end, bits, **opts)
     torch.cuda.synchronize()
     assert np.array_equal(to_host(d, keys.dtype), keys), "input was written"
     return to_host(out, keys.dtype)
 
 
-def run_pairs(rs, keys, vals, begin=0, end=None, bits=8):
+def run_pairs(rs, keys, vals, begin=0, end=None, bits=8, **opts):
     dk, dv = to_dev(keys), to_dev(vals)
     ko, vo = poisoned_like(dk), poisoned_like(dv)
-    rs.radix_sort_pairs(dk, dv, ko, vo, begin, end, bits)
+    rs.radix_sort_pairs(dk, dv, ko, vo, begin, end, bits, **opts)
     torch.cuda.synchronize()
     assert np.array_equal(to_host(dk, keys.dtype), keys), "input keys were written"
     assert np.array_equal(to_host(dv, vals.dtype), vals), "input payloads were written"
@@ -98,29 +98,25 @@ RAGGED = [1, 2, 31, 32, 33, 1000, TILE_U64 - 1, TILE_U64, TILE_U64 + 1, TILE_U64
           3 * TILE_U32_KEYS + 17, 100_003]
 
 
-@pytest.fixture(params=[True, False], ids=["one_kernel_short_rows", "multi_kernel_only"])
-def short_rows_one_kernel(rs, request):
-    """Inputs of at most rs.SMALL_SORT_MAX_KEYS keys are sorted by one kernel;
-    with it off the tile-boundary sizes below exercise the scatter and tail
-    kernels instead."""
-    rs.set_small_sort(request.param)
-    yield request.param
-    rs.set_small_sort(True)
-
-
 @pytest.mark.parametrize("n", RAGGED)
-def test_ragged_sizes(rs, n, short_rows_one_kernel):
+@pytest.mark.parametrize("small_sort", [True, False], ids=["one_kernel_short_rows",
+                                                          "multi_kernel_only"])
+def test_ragged_sizes(rs, n, small_sort):
+    # Inputs of at most rs.SMALL_SORT_MAX_KEYS keys are sorted by one kernel;
+    # with small_sort=False the tile-boundary sizes exercise the scatter
+    # kernels (full and partial tiles) instead.
+    o = {"small_sort": small_sort}
     keys = workloads.u32_uniform(n, 11)
     keys[::3] = keys[0]  # ties across tiles
     vals = workloads.index_payload(n)
     for bits in (8, 5):
-        ko, vo = run_pairs(rs, keys, vals, 0, 32, bits)
+        ko, vo = run_pairs(rs, keys, vals, 0, 32, bits, **o)
         ek, ev = oracle.sort(keys, vals, 0, 32, bits)
         assert_pairs(ko, vo, ek, ev, f"b={bits}")
-        assert np.array_equal(run_keys(rs, keys, 0, 32, bits), ek)
+        assert np.array_equal(run_keys(rs, keys, 0, 32, bits, **o), ek)
     k64 = workloads.u64_uniform(n, 12)
-    assert np.array_equal(run_keys(rs, k64, 0, 64, 8), oracle.sort(k64, None, 0, 64, 8)[0])
-    k64o, v64o = run_pairs(rs, k64, vals, 0, 64, 8)
+    assert np.array_equal(run_keys(rs, k64, 0, 64, 8, **o), oracle.sort(k64, None, 0, 64, 8)[0])
+    k64o, v64o = run_pairs(rs, k64, vals, 0, 64, 8, **o)
     e64, ev64 = oracle.sort(k64, vals, 0, 64, 8)
     assert_pairs(k64o, v64o, e64, ev64)
 
@@ -146,8 +142,8 @@ def test_bit_ranges(rs, begin, end, bits):
     keys = workloads.u32_uniform(n, 3)
     vals = workloads.index_payload(n)
     ko, vo = run_pairs(rs, keys, vals, begin, end, bits)
-    order = np.argsort(field(keys, begin, end), kind="stable")
-    assert np.array_equal(ko, keys[order]) and np.array_equal(vo, vals[order])
+    ek, ev = oracle.sort(keys, vals, begin, end, bits)
+    assert_pairs(ko, vo, ek, ev, f"bits [{begin}, {end}) b={bits}")
 
 
 def test_one_key_and_all_equal_small(rs):
@@ -155,7 +151,8 @@ def test_one_key_and_all_equal_small(rs):
         keys = np.full(n, 0xDEADBEEF, np.uint32)
         vals = workloads.index_payload(n)
         ko, vo = run_pairs(rs, keys, vals)
-        assert np.array_equal(ko, keys) and np.array_equal(vo, vals)
+        ek, ev = oracle.sort(keys, vals, 0, 32, 8)
+        assert_pairs(ko, vo, ek, ev, f"n={n}")
 
 
 def test_empty_input(rs):
@@ -232,7 +229,8 @@ def test_segmented_page_shape(rs, kind, descending):
 
 
 @pytest.mark.parametrize("shape", [(1, 1), (3, 1000), (64, 64), (7, 4097), (3, 8192), (3, 8193),
-                                   (2, 200_001),
+                                   (2, 2 * TILE_F16), (2, 2 * TILE_F16 + 1),
+                                   (3, 3 * TILE_F16 - 1), (2, 200_001),
                                    (16, 131072), (1024, 1), (5, 0), (0, 7)])
 @pytest.mark.parametrize("descending", [False, True])
 def test_segmented_shapes(rs, shape, descending):

@@ -2,7 +2,8 @@
 skipped on the device (the schedule comes from the upfront histograms).
 Parity with the oracle, and the number of passes run, for sorts with
 0, 1, 3 and 5 of their passes run, in and out of place, for keys, pairs,
-typed keys and row-wise 16-bit sorts."""
+typed keys and row-wise 16-bit sorts.  Pass skipping is an option of each
+call (pass_skipping=True), never a state of the library."""
 import numpy as np
 import pytest
 import torch
@@ -14,24 +15,19 @@ from tests.gpu_util import assert_pairs, poisoned_like, to_dev, to_host
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(autouse=True)
-def skipping(rs):
-    rs.set_pass_skipping(True)
-    yield
-    rs.set_pass_skipping(False)
-
-
-def sort_pairs(rs, keys, vals, begin, end, bits, in_place, **kw):
+def sort_pairs(rs, keys, vals, begin, end, bits, in_place, skip=True, **kw):
     dk, dv = to_dev(keys), to_dev(vals)
     kb = keys.dtype.itemsize
     temp = torch.empty(rs.temp_bytes(keys.size, kb, 4, begin, end, bits), dtype=torch.uint8,
                        device="cuda")
     if in_place:
-        rs.radix_sort_pairs(dk, dv, dk, dv, begin, end, bits, temp=temp, **kw)
+        rs.radix_sort_pairs(dk, dv, dk, dv, begin, end, bits, temp=temp, pass_skipping=skip,
+                            **kw)
         ko, vo = dk, dv
     else:
         ko, vo = poisoned_like(dk), poisoned_like(dv)
-        rs.radix_sort_pairs(dk, dv, ko, vo, begin, end, bits, temp=temp, **kw)
+        rs.radix_sort_pairs(dk, dv, ko, vo, begin, end, bits, temp=temp, pass_skipping=skip,
+                            **kw)
     run = rs.passes_run(temp)
     return to_host(ko, keys.dtype), to_host(vo, vals.dtype), run
 
@@ -42,7 +38,7 @@ def sort_keys(rs, keys, begin, end, bits, in_place, **kw):
     temp = torch.empty(rs.temp_bytes(keys.size, kb, 0, begin, end, bits), dtype=torch.uint8,
                        device="cuda")
     ko = dk if in_place else poisoned_like(dk)
-    rs.radix_sort_keys(dk, ko, begin, end, bits, temp=temp, **kw)
+    rs.radix_sort_keys(dk, ko, begin, end, bits, temp=temp, pass_skipping=True, **kw)
     return to_host(ko, keys.dtype), rs.passes_run(temp)
 
 
@@ -87,13 +83,12 @@ def test_skipped_passes_keys(rs, case, in_place):
 
 
 def test_skipping_off_runs_every_pass(rs):
-    rs.set_pass_skipping(False)
     make, begin, end, bits, _ = CASES["u32_const_byte"]
     keys = make(50_001)
     vals = workloads.index_payload(50_001)
     ek, ev = oracle.sort(keys, vals, begin, end, bits)
     for in_place in (False, True):
-        ko, vo, run = sort_pairs(rs, keys, vals, begin, end, bits, in_place)
+        ko, vo, run = sort_pairs(rs, keys, vals, begin, end, bits, in_place, skip=False)
         assert_pairs(ko, vo, ek, ev)
         assert run == 4
 
@@ -126,7 +121,7 @@ def _rows_sort(rs, x, descending, in_place=False):
     d = torch.from_numpy(x.view(np.int16)).cuda().view(torch.float16)
     temp = torch.empty(rs.segmented_temp_bytes(*x.shape), dtype=torch.uint8, device="cuda")
     vals = d if in_place else None
-    v, i = rs.segmented_sort(d, descending, values_out=vals, temp=temp)
+    v, i = rs.segmented_sort(d, descending, values_out=vals, temp=temp, pass_skipping=True)
     return v.view(torch.int16).cpu().numpy().view(np.uint16), i.cpu().numpy(), rs.passes_run(temp)
 
 

@@ -76,13 +76,9 @@ def test_small_sort_switch(rs):
     keys = workloads.u32_uniform(n, 17)
     vals = workloads.index_payload(n)
     ek, ev = oracle.sort(keys, vals, 0, 32, 8)
-    try:
-        for on in (False, True):
-            rs.set_small_sort(on)
-            dk, dv = to_dev(keys), to_dev(vals)
-            ko, vo = poisoned_like(dk), poisoned_like(dv)
-            rs.radix_sort_pairs(dk, dv, ko, vo, 0, 32, 8)
-            assert np.array_equal(to_host(ko, np.uint32), ek)
-            assert np.array_equal(to_host(vo, np.uint32), ev)
-    finally:
-        rs.set_small_sort(True)
+    for on in (False, True):
+        dk, dv = to_dev(keys), to_dev(vals)
+        ko, vo = poisoned_like(dk), poisoned_like(dv)
+        rs.radix_sort_pairs(dk, dv, ko, vo, 0, 32, 8, small_sort=on)
+        assert np.array_equal(to_host(ko, np.uint32), ek)
+        assert np.array_equal(to_host(vo, np.uint32), ev)

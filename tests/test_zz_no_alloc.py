@@ -1,10 +1,12 @@
 """The key-value sort for callers that cannot allocate device memory.
 
-Code that sorts inside a stream capture, or that is handed only its input
-and output buffers, cannot ask the driver for scratch.  The no-allocation
-entry point keeps its scratch in a fixed array of the library's device code
-instead; it must give exactly what the ordinary entry point gives, call after
-call, although every call reuses (and finds dirty) the same array.
+A caller whose device memory belongs to a pool it may not grow, or a plugin
+handed only its input and output buffers, cannot ask for scratch.  The
+no-allocation entry point keeps its scratch in a fixed array of the
+library's device code instead; it must give exactly what the ordinary entry
+point gives (and what the oracle gives), call after call, although every
+call reuses (and finds dirty) the same array, and its device-side status
+must be readable through its own status call.
 """
 import ctypes
 
@@ -12,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from lsd_radix_sort_gb300 import workloads
 from tests.gpu_util import poisoned_like, to_dev, to_host
 
@@ -39,10 +42,15 @@ def test_no_alloc_matches_ordinary_sort_twice(rs, n, begin, end, bits):
         dk, dv = to_dev(keys), to_dev(vals)
         ko, vo = poisoned_like(dk), poisoned_like(dv)
         assert call_noalloc(lib, dk, dv, ko, vo, n, begin, end, bits) == rs.RS_OK
-        ek, ev = rs.radix_sort_pairs(dk, dv, begin_bit=begin, end_bit=end, digit_bits=bits)
+        stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        assert lib.radix_sort_pairs_u32_noalloc_status(stream) == rs.RS_OK
+        gk, gv = rs.radix_sort_pairs(dk, dv, begin_bit=begin, end_bit=end, digit_bits=bits)
         torch.cuda.synchronize()
-        assert np.array_equal(to_host(ko, np.uint32), to_host(ek, np.uint32)), f"call {call}"
-        assert np.array_equal(to_host(vo, np.uint32), to_host(ev, np.uint32)), f"call {call}"
+        assert np.array_equal(to_host(ko, np.uint32), to_host(gk, np.uint32)), f"call {call}"
+        assert np.array_equal(to_host(vo, np.uint32), to_host(gv, np.uint32)), f"call {call}"
+        ek, ev = oracle.sort(keys, vals, begin, end, bits)
+        assert np.array_equal(to_host(ko, np.uint32), ek), f"call {call} vs oracle"
+        assert np.array_equal(to_host(vo, np.uint32), ev), f"call {call} vs oracle"
 
 
 def test_no_alloc_rejects_beyond_its_maximum(rs):
