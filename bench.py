@@ -357,8 +357,7 @@ def config_sorts(rs, torch, workloads, n_log2: int, peak: float, reps: int = 10)
 
     def entry(ms, nkeys, ideal, ok, **kw):
         d = {"ms": round(ms, 4), "gkeys_s": round(nkeys / ms / 1e6, 2),
-             "ideal_bytes": ideal, "hbm_frac": round(ideal / (ms * 1e-3) / 1e9 / peak, 4),
-             "checked": ok}
+             "hbm_frac": round(ideal / (ms * 1e-3) / 1e9 / peak, 4), "checked": ok}
         d.update(kw)
         return d
 
@@ -424,7 +423,8 @@ def config_sorts(rs, torch, workloads, n_log2: int, peak: float, reps: int = 10)
             ok = gathered and not bool((tv[:, 1:] < tv[:, :-1]).any()) and not bool(
                 ((tv[:, 1:] == tv[:, :-1]) & (i[:, 1:] < i[:, :-1])).any())
             out[f"rows_{kind}_{rows}x{cols}{'_desc' if desc else ''}"] = entry(
-                ms, rows * cols, rows * cols * 26, ok)
+                ms, rows * cols, rows * cols * 26, ok,
+                hbm_frac_formula=round(rows * cols * 42 / (ms * 1e-3) / 1e9 / peak, 4))
         del x, v, i, temp
     return out
 
@@ -467,6 +467,24 @@ def row_sorts(rs, torch, workloads, reps: int = 20):
     return out
 
 
+def host_cores() -> dict:
+    """The host's logical cores and the ones this process may run on."""
+    try:
+        usable = len(os.sched_getaffinity(0))
+    except Exception:
+        usable = os.cpu_count()
+    return {"logical": os.cpu_count(), "usable": usable}
+
+
+def _median_time(fn, reps: int) -> float:
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        fn()
+        times.append(time.perf_counter() - t0)
+    return statistics.median(times)
+
+
 def cpu_oracle_rate(n_sample: int, reps: int = 1):
     """Time the CPU oracle (as it stands, one thread) on a sample of the workload."""
     import oracle
@@ -474,12 +492,62 @@ def cpu_oracle_rate(n_sample: int, reps: int = 1):
     keys = workloads.u32_uniform(n_sample, 0)
     vals = workloads.index_payload(n_sample)
     oracle.build()
-    times = []
-    for _ in range(reps):
-        t0 = time.perf_counter()
-        oracle.sort(keys, vals, 0, 32, DIGIT_BITS)
-        times.append(time.perf_counter() - t0)
-    return n_sample / statistics.median(times) / 1e9, statistics.median(times)
+    secs = _median_time(lambda: oracle.sort(keys, vals, 0, 32, DIGIT_BITS), reps)
+    return n_sample / secs / 1e9, secs
+
+
+def cpu_config_rates(log2: int) -> dict:
+    """The oracle (one thread, as it stands) on a bounded sample of every
+    configuration, and numpy's stable sort of the headline keys on one core
+    (a library comparison sort, the CUDA Handbook's std::sort analogue).
+    Samples: 2^log2 keys for the 2^28 workloads (2^(log2-2) for 64-bit keys),
+    the small configurations whole; median of 3 runs below 2^24 keys, one
+    run above.  Rates in Gkeys/s."""
+    import oracle
+    from lsd_radix_sort_gb300 import workloads
+    oracle.build()
+    out = {}
+
+    def rate(name, n, fn, sample):
+        secs = _median_time(fn, 3 if n < (1 << 24) else 1)
+        out[name] = {"gkeys_s": n / secs / 1e9, "seconds": round(secs, 4), "sample": sample}
+
+    k = workloads.u32_small(1024, 0, 12)
+    rate("1024_keys_b4_bits0_12", 1024, lambda: oracle.sort(k, None, 0, 12, 4), "whole (1,024 keys)")
+    for bits in (4, 8):
+        k = workloads.u32_uniform(1 << 22, 0)
+        rate(f"2^22_keys_b{bits}", 1 << 22, lambda: oracle.sort(k, None, 0, 32, bits),
+             "whole (4,194,304 keys, seed 0)")
+    n = 1 << log2
+    k = workloads.u32_uniform(n, 0)
+    v = workloads.index_payload(n)
+    rate("u32_pairs_uniform", n, lambda: oracle.sort(k, v, 0, 32, 8), f"2^{log2} of 2^28 keys")
+    rate("u32_keys_uniform", n, lambda: oracle.sort(k, None, 0, 32, 8), f"2^{log2} of 2^28 keys")
+    t0 = time.perf_counter()
+    np.argsort(k, kind="stable")
+    secs = time.perf_counter() - t0
+    out["numpy_stable_argsort_u32_1core"] = {"gkeys_s": n / secs / 1e9, "seconds": round(secs, 4),
+                                             "sample": f"2^{log2} uniform u32 keys, one thread"}
+    for name, gen in workloads.U32_DISTRIBUTIONS.items():
+        if name == "uniform":
+            continue
+        kk = gen(1 << (log2 - 2), 0)
+        vv = workloads.index_payload(kk.size)
+        rate(f"u32_pairs_{name}", kk.size, lambda: oracle.sort(kk, vv, 0, 32, 8),
+             f"2^{log2 - 2} of 2^28 keys")
+    n64 = 1 << (log2 - 2)
+    v64 = workloads.index_payload(n64)
+    for name, gen, end in (("u64_pairs_uniform", workloads.u64_uniform, 64),
+                           ("u64_pairs_skewed", workloads.u64_skewed, 64),
+                           ("u64_pairs_bits0_39", workloads.u64_uniform, 40)):
+        kk = gen(n64, 0)
+        rate(name, n64, lambda: oracle.sort(kk, v64, 0, end, 8), f"2^{log2 - 2} of 2^28 keys")
+    rows = 64
+    for kind in ("f16", "bf16"):
+        x = workloads.rows16(rows, 65536, kind, 0)
+        rate(f"rows_{kind}_1024x65536", rows * 65536, lambda: oracle.segmented_sort16(x, False),
+             f"{rows} of 1024 rows")
+    return out
 
 
 def run_reference(args, rank, world):
@@ -543,10 +611,15 @@ def main():
     ap.add_argument("--no-small-sorts", action="store_true")
     ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--no-configs", action="store_true")
+    ap.add_argument("--no-cpu-configs", action="store_true")
+    ap.add_argument("--details", default=None,
+                    help="file for the bulky tables (default: gpurun_out/bench_details.json "
+                         "when that folder exists, else bench_details.json)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
     rank, world, local = dist_setup()
+    details = {}  # bulky tables, written beside the run instead of printed
     if args.impl == "reference":
         run_reference(args, rank, world)
         return
@@ -746,20 +819,29 @@ def main():
         pipe_steps = max(args.e2e_steps, 6)
         e_serial, serial_reps = timed_e2e(lambda i: serial_step(), args.e2e_steps)
         e_pipe, pipe_reps = timed_e2e(pipelined_step, pipe_steps)
-        # the results of the last step are the sort of the input
+        # The last step's result, as it came back to host memory, is checked
+        # whole on the device: keys in order, payloads a permutation that
+        # carries each input key, equal keys in input order.
         b = sets[(pipe_steps - 1) % nsets]
-        ok = bool(np.array_equal(b["hko"][:4096].numpy(), ko[:4096].cpu().numpy()))
+        for key in ("dk", "dv", "ko", "vo", "temp"):
+            for st in sets:
+                st[key] = None
+        hko_d, hvo_d = b["hko"].to(dev), b["hvo"].to(dev)
+        ok = _check_sorted_pairs(torch, dk, hko_d, hvo_d, None, _order_key(torch, hko_d, "u32"))
+        del hko_d, hvo_d
         e2e = {"value": world * n / (e_pipe * 1e-3) / 1e9, "unit": "Gkeys/s",
                "h2d_bytes_per_step": hk.numel() * 4 + hv.numel() * 4,
                "d2h_bytes_per_step": sets[0]["hko"].numel() * 4 + sets[0]["hvo"].numel() * 4,
                "ms_per_step": e_pipe, "mode": f"pipelined over {nsets} buffer sets (wall clock)",
                "timing": f"best of {E2E_REPS} repetitions of {pipe_steps} steps",
-               "reps_ms_per_step": [round(x, 3) for x in pipe_reps],
-               "result_checked": ok,
-               "host_link": {k: round(v, 1) for k, v in link.items()},
-               "serial": {"value": world * n / (e_serial * 1e-3) / 1e9, "ms_per_step": e_serial,
-                          "timing": f"best of {E2E_REPS} repetitions of {args.e2e_steps} steps",
-                          "reps_ms_per_step": [round(x, 3) for x in serial_reps]}}
+               "result_checked": ok, "result_check": "whole output, properties on the device",
+               "serial_value": world * n / (e_serial * 1e-3) / 1e9,
+               "host_link_gbs": {k: round(v, 1) for k, v in link.items()}}
+        details["e2e"] = {"reps_ms_per_step": [round(x, 3) for x in pipe_reps],
+                          "serial": {"ms_per_step": e_serial,
+                                     "timing": f"best of {E2E_REPS} repetitions of "
+                                               f"{args.e2e_steps} steps",
+                                     "reps_ms_per_step": [round(x, 3) for x in serial_reps]}}
         del hk, hv, sets
 
     # ---- the other key distributions of the same workload ----------------
@@ -775,14 +857,14 @@ def main():
                 del kk
                 dms = time_sorts(rs, torch, dk, dv, ko, vo, temp, max(args.steps // 2, 3), 3,
                                  stream)
-            dists[name] = {"ms": dms, "gkeys_s": n / (dms * 1e-3) / 1e9,
-                           "hbm_frac": total_ideal / (dms * 1e-3) / 1e9 / peak}
+            dists[name] = {"ms": round(dms, 4), "gkeys_s": round(n / (dms * 1e-3) / 1e9, 2),
+                           "hbm_frac": round(total_ideal / (dms * 1e-3) / 1e9 / peak, 4)}
             if name != "uniform":
                 # the same sort with pass skipping on: identity passes are not
                 # run, so the ideal-bytes model above does not apply
                 sms = time_sorts(rs, torch, dk, dv, ko, vo, temp, max(args.steps // 2, 3), 3,
                                  stream, pass_skipping=True)
-                dists[name]["pass_skipping"] = {"ms": sms, "gkeys_s": n / (sms * 1e-3) / 1e9,
+                dists[name]["pass_skipping"] = {"ms": round(sms, 4),
                                                 "passes_run": rs.passes_run(temp)}
 
     cfg_tab = None
@@ -791,18 +873,32 @@ def main():
     small = None
     keys_cfg = None
     if not args.no_small_sorts:
-        small = small_sort_latency(rs, torch, workloads, (10, 12, 13, 14, 16, 18, 20))
-        keys_cfg = keys_only_configs(rs, torch, workloads)
+        small_full = small_sort_latency(rs, torch, workloads, (10, 12, 13, 14, 16, 18, 20))
+        details["small_sorts"] = small_full
+        small = {k: [v["stream_us"], v["graph_us"]] for k, v in small_full.items()}
+        keys_full = keys_only_configs(rs, torch, workloads)
+        details["keys_only_configs"] = keys_full
+        keys_cfg = {k: {"gkeys_s_best": v["gkeys_s_best"],
+                        "checked": all(r["checked"] for r in v["seeds"])}
+                    for k, v in keys_full.items()}
     rows_tab = None
     if not args.no_rows:
-        rows_tab = row_sorts(rs, torch, workloads)
+        rows_full = row_sorts(rs, torch, workloads)
+        details["row_sorts"] = rows_full
+        rows_tab = {k: [v["lookback_ms"], v["precomputed_ms"], v["torch_sort_ms"]]
+                    for k, v in rows_full.items()}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         rate, secs = cpu_oracle_rate(1 << args.cpu_log2)
         cpu = {"value": rate, "unit": "Gkeys/s", "cores": 1, "kind": "oracle",
                "sample": f"2^{args.cpu_log2} keys of the same uniform u32 key-value workload, "
-                         f"one sort, {secs:.1f} s on one host thread"}
+                         f"one sort, {secs:.1f} s on one host thread",
+               "host_cores": host_cores()}
+        if not args.no_cpu_configs:
+            cpu_cfg = cpu_config_rates(args.cpu_log2 - 2)
+            details["cpu_baseline_configs"] = cpu_cfg
+            cpu["configs_gkeys_s"] = {k: round(v["gkeys_s"], 5) for k, v in cpu_cfg.items()}
 
     roofline["copy_probe_gbs"] = copy_gbs
     if rank == 0:
@@ -821,9 +917,17 @@ def main():
                         "frac_of_peak": total_ideal / (ms_max * 1e-3) / 1e9 / peak},
                 "e2e": e2e, "gpu_launches": launches, "kernels": kernels,
                 "roofline": roofline, "cpu_baseline": cpu, "clocks": clocks,
-                "distributions": dists, "configs": cfg_tab, "small_sorts": small,
-                "keys_only_configs": keys_cfg,
-                "row_sorts": rows_tab}
+                "distributions": dists, "configs": cfg_tab,
+                "small_sorts_us_stream_graph": small, "keys_only_configs": keys_cfg,
+                "row_sorts_ms_lookback_precomputed_torch": rows_tab}
+        path = args.details or os.path.join(ROOT, "gpurun_out", "bench_details.json")
+        try:
+            os.makedirs(os.path.dirname(path), exist_ok=True)
+            with open(path, "w") as f:
+                json.dump(details, f, indent=1)
+            line["details_file"] = os.path.relpath(path, ROOT)
+        except OSError:
+            line["details_file"] = None
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

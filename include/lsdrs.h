@@ -247,6 +247,23 @@ rs_status radix_sort_device_status(const void* temp, void* stream);
  *   passes  (host) receives the count (0 .. passes of the bit range) */
 rs_status radix_sort_passes_run(const void* temp, int* passes, void* stream);
 
+/* 1 when this library is the bounds-checked build (compiled with
+ * LSDRS_CHECKED=1: every shared and global index of the scatter, histogram
+ * and one-kernel sorts is tested before the access, and a failed test is
+ * recorded in the scratch header instead of performed), else 0.  A
+ * verification aid standing in for memory checkers; no counterpart on the
+ * pages. */
+int rs_checked_build(void);
+
+/* Bounds-checked builds: synchronises `stream`, writes the number of failed
+ * index tests recorded in `temp` since the last call (*count) and the site
+ * code of the first (*first_site, 0 if none), then clears both.  Clear them
+ * once before the first sort on a new scratch buffer.  Other builds record
+ * nothing, so after a clear the count stays 0.
+ *   temp  (device) scratch of a sort (at least 1 KiB) */
+rs_status radix_sort_checked_violations(void* temp, void* stream, uint32_t* count,
+                                        uint32_t* first_site);
+
 /* Human-readable name of a status code (static storage). */
 const char* rs_status_string(rs_status status);
 

@@ -29,7 +29,8 @@ __all__ = [
     "radix_sort_pairs", "segmented_sort", "segmented_temp_bytes", "upfront_histograms",
     "device_status", "passes_run", "SMALL_SORT_MAX_KEYS", "copy_probe",
     "lookback_timeout_probe", "profile_enable", "profile_read", "launch_count_reset",
-    "noalloc_status", "EXPORTED_SYMBOLS", "RS_MAX_KEYS", "RS_MAX_ROW_KEYS",
+    "noalloc_status", "EXPORTED_SYMBOLS", "RS_MAX_KEYS", "RS_MAX_ROW_KEYS", "checked_build",
+    "BoundsViolation",
 ]
 
 RS_OK, RS_ERR_INVALID, RS_ERR_TEMP_TOO_SMALL, RS_ERR_CUDA, RS_ERR_LOOKBACK_TIMEOUT = range(5)
@@ -55,6 +56,7 @@ EXPORTED_SYMBOLS = (
     "rs_copy_probe", "rs_profile_enable", "rs_profile_read", "rs_launch_count_reset",
     "radix_sort_pairs_u32_noalloc", "radix_sort_pairs_u32_noalloc_status",
     "radix_sort_keys_typed", "radix_sort_pairs_typed", "radix_sort_passes_run",
+    "rs_checked_build", "radix_sort_checked_violations",
 )
 
 
@@ -130,6 +132,7 @@ def load_library() -> ctypes.CDLL:
             "radix_sort_keys_typed": [i, i, P, P, sz, i, i, i, P, sz, P, P],
             "radix_sort_passes_run": [P, P, P],
             "radix_sort_pairs_typed": [i, i, P, P, P, P, sz, i, i, i, P, sz, P, P],
+            "radix_sort_checked_violations": [P, P, P, P],
         }
         for name, args in sig.items():
             f = getattr(lib, name)
@@ -141,6 +144,8 @@ def load_library() -> ctypes.CDLL:
         lib.rs_profile_read.restype = i
         lib.rs_launch_count_reset.argtypes = []
         lib.rs_launch_count_reset.restype = u64
+        lib.rs_checked_build.argtypes = []
+        lib.rs_checked_build.restype = i
         _lib = lib
         return lib
 
@@ -155,6 +160,45 @@ def _status_name(status: int) -> str:
 def _check(status: int, what: str):
     if status != RS_OK:
         raise RadixSortError(status, what)
+
+
+class BoundsViolation(RuntimeError):
+    """A bounds-checked build recorded failed index tests during a sort."""
+
+
+def checked_build() -> bool:
+    """True when the loaded library is the bounds-checked build."""
+    return bool(load_library().rs_checked_build())
+
+
+def _violations(t, stream):
+    count, site = ctypes.c_uint32(0), ctypes.c_uint32(0)
+    _check(load_library().radix_sort_checked_violations(_ptr(t), _stream_ptr(stream),
+                                                        ctypes.byref(count), ctypes.byref(site)),
+           "radix_sort_checked_violations")
+    return count.value, site.value
+
+
+class _BoundsGuard:
+    """Around one sort with a bounds-checked library: clear the scratch's
+    violation words before, raise BoundsViolation if any test failed."""
+
+    def __init__(self, t, stream, what):
+        self.t, self.stream, self.what = t, stream, what
+        self.on = checked_build()
+
+    def __enter__(self):
+        if self.on:
+            _violations(self.t, self.stream)
+        return self
+
+    def __exit__(self, *exc):
+        if self.on and exc[0] is None:
+            count, site = _violations(self.t, self.stream)
+            if count:
+                raise BoundsViolation(f"{self.what}: {count} index tests failed "
+                                      f"(first at site {site})")
+        return False
 
 
 def _stream_ptr(stream=None):
@@ -258,16 +302,17 @@ def radix_sort_keys(keys, out=None, begin_bit: int = 0, end_bit: int | None = No
     tb = temp_bytes(n, kb, 0, begin_bit, end_bit, digit_bits)
     t = _temp(tb, keys.device, temp)
     tsz = t.numel() * t.element_size()
-    if code is None:
-        f = lib.radix_sort_keys_u32 if kb == 4 else lib.radix_sort_keys_u64
-        st = f(_ptr(keys), _ptr(out), n, begin_bit, end_bit, digit_bits, _ptr(t), tsz,
-               _stream_ptr(stream))
-    else:
-        st = lib.radix_sort_keys_typed(code, int(descending), _ptr(keys), _ptr(out), n, begin_bit,
-                                       end_bit, digit_bits, _ptr(t), tsz,
-                                       ctypes.byref(opts) if opts is not None else None,
-                                       _stream_ptr(stream))
-    _check(st, "radix_sort_keys")
+    with _BoundsGuard(t, stream, "radix_sort_keys"):
+        if code is None:
+            f = lib.radix_sort_keys_u32 if kb == 4 else lib.radix_sort_keys_u64
+            st = f(_ptr(keys), _ptr(out), n, begin_bit, end_bit, digit_bits, _ptr(t), tsz,
+                   _stream_ptr(stream))
+        else:
+            st = lib.radix_sort_keys_typed(code, int(descending), _ptr(keys), _ptr(out), n, begin_bit,
+                                           end_bit, digit_bits, _ptr(t), tsz,
+                                           ctypes.byref(opts) if opts is not None else None,
+                                           _stream_ptr(stream))
+        _check(st, "radix_sort_keys")
     return out
 
 
@@ -299,17 +344,18 @@ def radix_sort_pairs(keys, values, keys_out=None, values_out=None, begin_bit: in
     tb = temp_bytes(n, kb, 4, begin_bit, end_bit, digit_bits)
     t = _temp(tb, keys.device, temp)
     tsz = t.numel() * t.element_size()
-    if code is None:
-        f = lib.radix_sort_pairs_u32 if kb == 4 else lib.radix_sort_pairs_u64
-        st = f(_ptr(keys), _ptr(keys_out), _ptr(values), _ptr(values_out), n, begin_bit, end_bit,
-               digit_bits, _ptr(t), tsz, _stream_ptr(stream))
-    else:
-        st = lib.radix_sort_pairs_typed(code, int(descending), _ptr(keys), _ptr(keys_out),
-                                        _ptr(values), _ptr(values_out), n, begin_bit, end_bit,
-                                        digit_bits, _ptr(t), tsz,
-                                        ctypes.byref(opts) if opts is not None else None,
-                                        _stream_ptr(stream))
-    _check(st, "radix_sort_pairs")
+    with _BoundsGuard(t, stream, "radix_sort_pairs"):
+        if code is None:
+            f = lib.radix_sort_pairs_u32 if kb == 4 else lib.radix_sort_pairs_u64
+            st = f(_ptr(keys), _ptr(keys_out), _ptr(values), _ptr(values_out), n, begin_bit, end_bit,
+                   digit_bits, _ptr(t), tsz, _stream_ptr(stream))
+        else:
+            st = lib.radix_sort_pairs_typed(code, int(descending), _ptr(keys), _ptr(keys_out),
+                                            _ptr(values), _ptr(values_out), n, begin_bit, end_bit,
+                                            digit_bits, _ptr(t), tsz,
+                                            ctypes.byref(opts) if opts is not None else None,
+                                            _stream_ptr(stream))
+        _check(st, "radix_sort_pairs")
     return keys_out, values_out
 
 
@@ -348,16 +394,17 @@ def segmented_sort(x, descending: bool = False, values_out=None, indices_out=Non
     tb = segmented_temp_bytes(rows, cols)
     t = _temp(tb, x.device, temp)
     opts = _options(pass_skipping, tile_offsets, small_sort, lookback_timeout_ns)
-    if opts is None:
-        st = lib.radix_segmented_sort_f16(_ptr(x), _ptr(vals), _ptr(idx), rows, cols, kind,
-                                          int(bool(descending)), _ptr(t),
-                                          t.numel() * t.element_size(), _stream_ptr(stream))
-    else:
-        st = lib.radix_segmented_sort_f16_ex(_ptr(x), _ptr(vals), _ptr(idx), rows, cols, kind,
-                                             int(bool(descending)), _ptr(t),
-                                             t.numel() * t.element_size(), ctypes.byref(opts),
-                                             _stream_ptr(stream))
-    _check(st, "radix_segmented_sort_f16")
+    with _BoundsGuard(t, stream, "radix_segmented_sort_f16"):
+        if opts is None:
+            st = lib.radix_segmented_sort_f16(_ptr(x), _ptr(vals), _ptr(idx), rows, cols, kind,
+                                              int(bool(descending)), _ptr(t),
+                                              t.numel() * t.element_size(), _stream_ptr(stream))
+        else:
+            st = lib.radix_segmented_sort_f16_ex(_ptr(x), _ptr(vals), _ptr(idx), rows, cols, kind,
+                                                 int(bool(descending)), _ptr(t),
+                                                 t.numel() * t.element_size(), ctypes.byref(opts),
+                                                 _stream_ptr(stream))
+        _check(st, "radix_segmented_sort_f16")
     return vals, idx
 
 
@@ -376,10 +423,11 @@ def upfront_histograms(keys, begin_bit: int = 0, end_bit: int | None = None,
     t = _temp(tb, keys.device)
     hist = torch.empty((max(passes, 1), 1 << digit_bits), dtype=torch.int32, device=keys.device)
     bases = torch.empty_like(hist)
-    _check(lib.radix_sort_histograms(_ptr(keys), kb, n, begin_bit, end_bit, digit_bits,
-                                     _ptr(hist), _ptr(bases), _ptr(t),
-                                     t.numel() * t.element_size(), _stream_ptr(stream)),
-           "radix_sort_histograms")
+    with _BoundsGuard(t, stream, "radix_sort_histograms"):
+        _check(lib.radix_sort_histograms(_ptr(keys), kb, n, begin_bit, end_bit, digit_bits,
+                                         _ptr(hist), _ptr(bases), _ptr(t),
+                                         t.numel() * t.element_size(), _stream_ptr(stream)),
+               "radix_sort_histograms")
     return hist[:passes], bases[:passes]
 
 

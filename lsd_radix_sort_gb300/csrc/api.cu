@@ -592,6 +592,23 @@ rs_status radix_sort_device_status(const void* temp, void* stream) {
   return word == kErrNone ? RS_OK : static_cast<rs_status>(word);
 }
 
+int rs_checked_build(void) { return LSDRS_CHECKED; }
+
+rs_status radix_sort_checked_violations(void* temp, void* stream, uint32_t* count,
+                                        uint32_t* first_site) {
+  if (!temp || !count || !first_site) return RS_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t* w = static_cast<uint32_t*>(temp) + kHdrViolations;
+  uint32_t h[2] = {0, 0};
+  if (cudaMemcpyAsync(h, w, sizeof(h), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return RS_ERR_CUDA;
+  if (cudaMemsetAsync(w, 0, sizeof(h), s) != cudaSuccess) return RS_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RS_ERR_CUDA;
+  *count = h[0];
+  *first_site = h[1];
+  return RS_OK;
+}
+
 rs_status radix_sort_passes_run(const void* temp, int* passes, void* stream) {
   if (!temp || !passes) return RS_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

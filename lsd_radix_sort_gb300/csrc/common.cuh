@@ -6,9 +6,59 @@
 
 #include "../../include/lsdrs.h"
 
+// Programmatic dependent launch between the kernels of one sort: each
+// kernel is launched with programmatic stream serialisation, so the next
+// kernel of the stream may be scheduled while this one drains; every kernel
+// waits for its predecessors' completion and memory before its first global
+// access (griddepcontrol.wait), so the order of memory operations is that of
+// plain stream order.  0 launches plainly (A/B builds).
+#ifndef LSDRS_PDL
+#define LSDRS_PDL 1
+#endif
+
+// Bounds-checked build (LSDRS_CHECKED=1): every shared and global index of
+// the scatter, histogram and small-sort kernels is tested before the access;
+// a failed test is recorded in the scratch header and the access is skipped.
+#ifndef LSDRS_CHECKED
+#define LSDRS_CHECKED 0
+#endif
+
 namespace lsdrs {
 
 constexpr int kWarp = 32;
+
+// First statement of every kernel of a sort: wait for the grids this one
+// depends on (a no-op when launched without the attribute), then let the
+// next grid of the stream be scheduled.
+__device__ __forceinline__ void grid_dependency_sync() {
+#if LSDRS_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+
+// Host: launch `kern` with programmatic stream serialisation (LSDRS_PDL),
+// else with a plain launch.  Returns the launch error.
+template <class... KArgs, class... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t s, Args&&... args) {
+#if LSDRS_PDL
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+#else
+  kern<<<grid, block, smem, s>>>(static_cast<KArgs>(args)...);
+  return cudaGetLastError();
+#endif
+}
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 // Look-back status word: [P:1][A:1][value] in 32 bits (30-bit value) or 64
@@ -130,6 +180,27 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     if (mbar_try_wait(bar, parity)) return true;
     if (global_timer_ns() - t0 > timeout_ns) return false;
   }
+}
+
+// Scratch-header words of a bounds-checked build: the number of index tests
+// that failed and the site (a small code per access) of the first one.
+constexpr int kHdrViolations = 192;
+
+// Index test of a bounds-checked build: true when `ok`; otherwise counts
+// the failure in the scratch header and returns false, so that the caller
+// skips the access.  Always true in other builds.
+__device__ __forceinline__ bool in_bounds(bool ok, uint32_t* header, uint32_t site) {
+#if LSDRS_CHECKED
+  if (!ok) {
+    atomicAdd(header + kHdrViolations, 1u);
+    atomicCAS(header + kHdrViolations + 1, 0u, site);
+  }
+  return ok;
+#else
+  (void)header;
+  (void)site;
+  return true;
+#endif
 }
 
 __host__ __device__ constexpr inline size_t align_up(size_t x, size_t a) {

@@ -16,6 +16,7 @@ template <int Q>
 __global__ void __launch_bounds__(kScanThreads * Q) digit_scan_kernel(ScanArgs a) {
   __shared__ uint32_t part[Q][kScanThreads];
   __shared__ uint32_t warp_sums[kScanThreads / kWarp];
+  grid_dependency_sync();
   const int tid = threadIdx.x;
   const int d = tid % kScanThreads;  // digit (when < radix)
   const int q = tid / kScanThreads;  // share of the chunks
@@ -139,10 +140,9 @@ cudaError_t launch_hist(KeyKind k, int bits, const HistArgs& a, int grid, cudaSt
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s) {
   const int64_t grid = a.rows * a.passes;
   if (a.chunks_per_row >= 16)
-    digit_scan_kernel<4><<<static_cast<unsigned>(grid), kScanThreads * 4, 0, s>>>(a);
-  else
-    digit_scan_kernel<1><<<static_cast<unsigned>(grid), kScanThreads, 0, s>>>(a);
-  return cudaGetLastError();
+    return launch_kernel(digit_scan_kernel<4>, static_cast<unsigned>(grid), kScanThreads * 4, 0,
+                         s, a);
+  return launch_kernel(digit_scan_kernel<1>, static_cast<unsigned>(grid), kScanThreads, 0, s, a);
 }
 
 }  // namespace lsdrs

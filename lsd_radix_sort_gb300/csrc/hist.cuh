@@ -54,15 +54,16 @@ struct KeyCounter {
   static constexpr bool kHeld = MP <= 16;
   static constexpr int MH = kHeld ? MP : 1;
   uint32_t* col;
+  uint32_t* hdr;  // scratch header (bounds-checked builds record failures there)
   int begin_bit, passes;
   uint32_t last_mask;
   KeyXform xf;
   int shift[MH];
   uint32_t mask[MH];
 
-  __device__ __forceinline__ KeyCounter(uint32_t* c, int b, int np, uint32_t lm,
+  __device__ __forceinline__ KeyCounter(uint32_t* c, uint32_t* h, int b, int np, uint32_t lm,
                                         const KeyXform& x)
-      : col(c), begin_bit(b), passes(np), last_mask(lm), xf(x) {
+      : col(c), hdr(h), begin_bit(b), passes(np), last_mask(lm), xf(x) {
 #pragma unroll
     for (int p = 0; p < MH; ++p) {
       shift[p] = b + p * BITS;
@@ -76,21 +77,21 @@ struct KeyCounter {
       for (int p = 0; p < MP; ++p) {
         const uint32_t w = static_cast<uint32_t>(t >> (32 * (p / 4)));
         const uint32_t d = __byte_perm(w, 0u, 0x4440u + (p & 3));
-        atomicAdd(col + (p * R + d) * C, 1u);
+        if (in_bounds(d < R, hdr, 10)) atomicAdd(col + (p * R + d) * C, 1u);
       }
     } else if constexpr (kHeld) {
 #pragma unroll
       for (int p = 0; p < MP; ++p) {
         if (ALL || p < passes) {
           const uint32_t d = KeyOp::digit(k, shift[p], mask[p], xf);
-          atomicAdd(col + (p * R + d) * C, 1u);
+          if (in_bounds(d < R && p < passes, hdr, 11)) atomicAdd(col + (p * R + d) * C, 1u);
         }
       }
     } else {
       for (int p = 0; p < passes; ++p) {
         const uint32_t m = p == passes - 1 ? last_mask : static_cast<uint32_t>(R - 1);
         const uint32_t d = KeyOp::digit(k, begin_bit + p * BITS, m, xf);
-        atomicAdd(col + (p * R + d) * C, 1u);
+        if (in_bounds(d < R, hdr, 12)) atomicAdd(col + (p * R + d) * C, 1u);
       }
     }
   }
@@ -101,7 +102,7 @@ struct KeyCounter {
 // scalar tail.
 template <class KeyOp, int BITS, bool ALL, bool BYTES>
 __device__ __forceinline__ void count_range(const typename KeyOp::T* base, int64_t begin,
-                                            int64_t end,
+                                            int64_t end, int64_t cols,
                                             const KeyCounter<KeyOp, BITS, ALL, BYTES>& c) {
   using T = typename KeyOp::T;
   using Cfg = HistCfg<KeyOp, BITS>;
@@ -114,14 +115,18 @@ __device__ __forceinline__ void count_range(const typename KeyOp::T* base, int64
   const int64_t body_begin = begin + head;
   const int64_t nvec = (end - body_begin) / V;
   const int64_t body_end = body_begin + nvec * V;
-  if (tid < head) c.add(base[begin + tid]);
-  if (tid < end - body_end) c.add(base[body_end + tid]);
+  if (tid < head && in_bounds(begin + tid < cols, c.hdr, 13)) c.add(base[begin + tid]);
+  if (tid < end - body_end && in_bounds(body_end + tid < cols, c.hdr, 14))
+    c.add(base[body_end + tid]);
   const uint4* vp = reinterpret_cast<const uint4*>(base + body_begin);
   int64_t v = tid;
   for (; v + (U - 1) * kHistThreads < nvec; v += U * kHistThreads) {
     uint4 buf[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) buf[u] = __ldcs(vp + v + u * kHistThreads);
+    for (int u = 0; u < U; ++u)
+      buf[u] = in_bounds(body_begin + (v + u * kHistThreads + 1) * V <= cols, c.hdr, 15)
+                   ? __ldcs(vp + v + u * kHistThreads)
+                   : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const T* ks = reinterpret_cast<const T*>(&buf[u]);
@@ -130,6 +135,7 @@ __device__ __forceinline__ void count_range(const typename KeyOp::T* base, int64
     }
   }
   for (; v < nvec; v += kHistThreads) {
+    if (!in_bounds(body_begin + (v + 1) * V <= cols, c.hdr, 16)) continue;
     uint4 b = __ldcs(vp + v);
     const T* ks = reinterpret_cast<const T*>(&b);
 #pragma unroll
@@ -144,6 +150,7 @@ __global__ void __launch_bounds__(kHistThreads, 1) upfront_hist_kernel(HistArgs 
   constexpr int R = Cfg::kRadix;
   constexpr int C = Cfg::kCols;
   extern __shared__ __align__(16) uint32_t cnt[];
+  grid_dependency_sync();
 
   const int tid = threadIdx.x;
   const int nb = a.passes * R;
@@ -154,7 +161,7 @@ __global__ void __launch_bounds__(kHistThreads, 1) upfront_hist_kernel(HistArgs 
     const size_t stride = static_cast<size_t>(gridDim.x) * kHistThreads;
     for (size_t i = static_cast<size_t>(blockIdx.x) * kHistThreads + tid; i < a.zero_words;
          i += stride)
-      a.zero_ptr[i] = 0;
+      if (i < kHdrViolations || i >= kHdrViolations + 2) a.zero_ptr[i] = 0;
   }
   __syncthreads();
 
@@ -168,15 +175,17 @@ __global__ void __launch_bounds__(kHistThreads, 1) upfront_hist_kernel(HistArgs 
   uint32_t* col = cnt + (tid & (C - 1));
   if (begin < end) {
     if (BITS == 8 && a.passes == Cfg::kMaxPasses && a.begin_bit == 0 && a.last_mask == 0xFFu) {
-      const KeyCounter<KeyOp, BITS, true, BITS == 8> c(col, a.begin_bit, a.passes, a.last_mask,
-                                                       a.xf);
-      count_range(base, begin, end, c);
+      const KeyCounter<KeyOp, BITS, true, BITS == 8> c(col, a.zero_ptr, a.begin_bit, a.passes,
+                                                       a.last_mask, a.xf);
+      count_range(base, begin, end, a.cols, c);
     } else if (a.passes == Cfg::kMaxPasses) {
-      const KeyCounter<KeyOp, BITS, true> c(col, a.begin_bit, a.passes, a.last_mask, a.xf);
-      count_range(base, begin, end, c);
+      const KeyCounter<KeyOp, BITS, true> c(col, a.zero_ptr, a.begin_bit, a.passes, a.last_mask,
+                                            a.xf);
+      count_range(base, begin, end, a.cols, c);
     } else {
-      const KeyCounter<KeyOp, BITS, false> c(col, a.begin_bit, a.passes, a.last_mask, a.xf);
-      count_range(base, begin, end, c);
+      const KeyCounter<KeyOp, BITS, false> c(col, a.zero_ptr, a.begin_bit, a.passes, a.last_mask,
+                                             a.xf);
+      count_range(base, begin, end, a.cols, c);
     }
   }
   __syncthreads();
@@ -200,8 +209,7 @@ cudaError_t launch_hist_t(const HistArgs& a, int grid, cudaStream_t s) {
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  kern<<<grid, kHistThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(kern, grid, kHistThreads, smem, s, a);
 }
 
 template <class KeyOp>

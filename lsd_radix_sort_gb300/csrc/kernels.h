@@ -121,6 +121,9 @@ constexpr int kHdrScanDone = 65;       // K-SCAN CTAs finished
 constexpr int kHdrPassesRun = 66;      // passes the schedule executes
 constexpr int kHdrNontrivial = 128;    // + pass: some row has two digits in it
 constexpr int kMaxPasses = 64;
+// Words kHdrViolations.. (common.cuh): bounds-checked builds' failed index
+// tests; K-HIST's zeroing skips them, radix_sort_checked_violations reads
+// and clears them.
 
 // Buffers a pass reads or writes: the caller's input, the scratch
 // ping-pong buffer, the caller's output.

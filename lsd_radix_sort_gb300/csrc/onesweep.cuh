@@ -68,18 +68,6 @@
 #ifndef LSDRS_STATS
 #define LSDRS_STATS 0
 #endif
-// Where a tile runs its look-back: 0 after staging its keys and payloads,
-// 1 after the digit scan (before staging), 2 as soon as it has published
-// its own counts (the earliest point; successors then see inclusive prefixes
-// sooner and walk back fewer tiles).
-#ifndef LSDRS_LB_EARLY
-#define LSDRS_LB_EARLY 0
-#endif
-// Per-warp digit counters and offsets held in 16 bits (two per shared word)
-// instead of 32.
-#ifndef LSDRS_CNT16
-#define LSDRS_CNT16 1
-#endif
 // Whole-byte digits by one byte permute (8-bit digits starting at a multiple
 // of 8) instead of shift and mask.
 #ifndef LSDRS_BYTE_DIGITS
@@ -200,7 +188,8 @@ __device__ __forceinline__ SW look_back(const SW* col, int64_t t, uint32_t* erro
     SW v[WIN];
     if (pt >= WIN - 1) {
 #pragma unroll
-      for (int k = 0; k < WIN; ++k) v[k] = ld_relaxed(p - k * R);
+      for (int k = 0; k < WIN; ++k)
+        v[k] = in_bounds(pt - k >= 0, error, 8) ? ld_relaxed(p - k * R) : LW::kFlagP;
     } else {
 #pragma unroll
       for (int k = 0; k < WIN; ++k) v[k] = k <= pt ? ld_relaxed(p - k * R) : LW::kFlagP;
@@ -227,11 +216,9 @@ __device__ __forceinline__ SW look_back(const SW* col, int64_t t, uint32_t* erro
 }
 
 // Shared-memory arrays every tile needs besides its key/payload buffers.
-// Per-warp counts and offsets stay below the tile size (< 2^16).
-using WarpCount = std::conditional_t<LSDRS_CNT16 != 0, uint16_t, uint32_t>;
 template <int W, int R>
 struct TileScratch {
-  alignas(16) WarpCount warp_cnt[W][R];  // per-warp digit counters, then per-warp offsets
+  alignas(16) uint32_t warp_cnt[W][R];  // per-warp digit counters, then per-warp offsets
   uint32_t warp_tot[W];     // per-warp sums of the digit-count scan
   uint32_t g_off[R];        // output position of staged slot j is g_off[d] + j
   uint32_t code;            // this pass's schedule code (kCode* bits)
@@ -327,7 +314,11 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   T keys[ITEMS];
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i)
-    keys[i] = (FULL || wpos + i * kWarp < valid) ? io.key_src[wpos + i * kWarp] : T(0);
+    keys[i] = ((FULL || wpos + i * kWarp < valid) &&
+               in_bounds(wpos + i * kWarp < valid && tile_begin + wpos + i * kWarp < a.cols,
+                         a.error, 1))
+                  ? io.key_src[wpos + i * kWarp]
+                  : T(0);
 
   // ---- 3. rank within the warp ------------------------------------------
   // The rank of item i among the warp's keys of its digit (below
@@ -336,7 +327,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   // keep the tile's state in registers.
   constexpr int NP = (ITEMS + 1) / 2;
   uint32_t packed[NP];
-  WarpCount* wc = s.warp_cnt[warp];
+  uint32_t* wc = s.warp_cnt[warp];
   const uint32_t lt = lanemask_lt();
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
@@ -346,9 +337,10 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     // Every peer lane reads the warp's count of its digit (one word per
     // digit, so a broadcast) and, after a warp barrier, stores the advanced
     // count: the peers write the same value to the same word.
-    const uint32_t before = wc[d];
+    const bool d_ok = in_bounds(d < R, a.error, 2);
+    const uint32_t before = d_ok ? wc[d] : 0u;
     __syncwarp();
-    wc[d] = static_cast<WarpCount>(before + __popc(peers));
+    if (d_ok) wc[d] = before + __popc(peers);
     __syncwarp();
     const uint32_t rank = before + __popc(peers & lt);
     if (i & 1)
@@ -367,25 +359,13 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   // thread d walks column d, so the column accesses are conflict-free).
   uint32_t my_count = 0;  // this tile's count of digit tid (without padding)
   uint32_t start = 0;     // first slot of digit tid in the tile
-  // ---- 6. decoupled look-back (thread d, digit d) ------------------------
-  // Sums the counts of the row's earlier tiles up to the first inclusive
-  // prefix and publishes this tile's inclusive prefix.  Run where
-  // LSDRS_LB_EARLY places it.  (PRE: the tile's output offsets were
-  // computed before the pass from per-tile digit counts: nothing to wait for.)
-  SW lb_excl = 0;
-  auto look_back_digit = [&]() {
-    if (!PRE && tid < R && t > 0) {
-      lb_excl = look_back<R, WIN>(status_row + tid, t, a.error, a.timeout_ns, trips, polls);
-      if (FULL) st_relaxed(status_tile + tid, LW::kFlagP | (lb_excl + my_count));
-    }
-  };
   {
     uint32_t total = 0;
     if (tid < R) {
 #pragma unroll
       for (int w = 0; w < W; ++w) {
         const uint32_t c = s.warp_cnt[w][tid];
-        s.warp_cnt[w][tid] = static_cast<WarpCount>(total);
+        s.warp_cnt[w][tid] = total;
         total += c;
       }
       my_count = (!FULL && tid == R - 1) ? total - static_cast<uint32_t>(TILE - valid) : total;
@@ -393,7 +373,6 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
       if (FULL && !PRE)
         st_relaxed(status_tile + tid, (t == 0 ? LW::kFlagP : LW::kFlagA) | SW(my_count));
     }
-    if (LSDRS_LB_EARLY == 2) look_back_digit();
     uint32_t incl = total;
 #pragma unroll
     for (int o = 1; o < kWarp; o <<= 1) {
@@ -410,13 +389,11 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     start = before + incl - total;
     if (tid < R) {
 #pragma unroll
-      for (int w = 0; w < W; ++w)
-        s.warp_cnt[w][tid] = static_cast<WarpCount>(s.warp_cnt[w][tid] + start);
+      for (int w = 0; w < W; ++w) s.warp_cnt[w][tid] += start;
     }
   }
   __syncthreads();
   LSDRS_PHASE(2);  // digit scan
-  if (LSDRS_LB_EARLY == 1) look_back_digit();
 
   // ---- 5. stage keys, then payloads, in tile-sorted order ---------------
   auto half = [](uint32_t w, int i) -> uint32_t { return (i & 1) ? (w >> 16) : (w & 0xFFFFu); };
@@ -430,11 +407,14 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
 #pragma unroll
   for (int k = 0; k < NP; ++k) {
     const int i0 = 2 * k, i1 = 2 * k + 1;
-    const uint32_t o0 = s.warp_cnt[warp][item_digit(i0)];
-    const uint32_t o1 = i1 < ITEMS ? s.warp_cnt[warp][item_digit(i1)] : 0u;
+    const uint32_t d0 = item_digit(i0);
+    const uint32_t d1 = i1 < ITEMS ? item_digit(i1) : 0u;
+    const uint32_t o0 = in_bounds(d0 < R, a.error, 2) ? s.warp_cnt[warp][d0] : 0u;
+    const uint32_t o1 = (i1 < ITEMS && in_bounds(d1 < R, a.error, 2)) ? s.warp_cnt[warp][d1] : 0u;
     const uint32_t pos = packed[k] + __byte_perm(o0, o1, 0x5410);
-    io.stage_keys[pos & 0xFFFFu] = keys[i0];
-    if (i1 < ITEMS) io.stage_keys[pos >> 16] = keys[i1];
+    if (in_bounds((pos & 0xFFFFu) < TILE, a.error, 3)) io.stage_keys[pos & 0xFFFFu] = keys[i0];
+    if (i1 < ITEMS && in_bounds((pos >> 16) < TILE, a.error, 3))
+      io.stage_keys[pos >> 16] = keys[i1];
     packed[k] = pos;
   }
   if constexpr (kVals) {
@@ -454,21 +434,31 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
       const int p = wpos + i * kWarp;
-      v[i] = !vin ? static_cast<uint32_t>(tile_begin + p) : ((FULL || p < valid) ? io.vals[p] : 0u);
+      v[i] = !vin ? static_cast<uint32_t>(tile_begin + p)
+                  : (((FULL || p < valid) && in_bounds(p < TILE, a.error, 4)) ? io.vals[p] : 0u);
     }
     __syncthreads();
 #pragma unroll
-    for (int i = 0; i < ITEMS; ++i) io.vals[half(packed[i >> 1], i)] = v[i];
+    for (int i = 0; i < ITEMS; ++i)
+      if (in_bounds(half(packed[i >> 1], i) < TILE, a.error, 5))
+        io.vals[half(packed[i >> 1], i)] = v[i];
   }
   LSDRS_PHASE(3);  // staging (thread 0's share)
 
-  // ---- output offset of each digit's run ---------------------------------
-  if (LSDRS_LB_EARLY == 0) look_back_digit();
+  // ---- 6. decoupled look-back (thread d, digit d) ------------------------
+  // Sums the counts of the row's earlier tiles up to the first inclusive
+  // prefix and publishes this tile's inclusive prefix.  (PRE: the tile's
+  // output offsets were computed before the pass from per-tile digit counts,
+  // so there is nothing to wait for.)  Output positions are below 2^32.
   if (PRE && tid < R) {
     s.g_off[tid] = a.offsets[(row * a.tiles_per_row + t) * R + tid] - start;
   } else if (tid < R) {
-    // output positions are below 2^32 (flat sorts) or 2^30 (rows)
-    s.g_off[tid] = a.bases[row * a.bases_row_stride + tid] + static_cast<uint32_t>(lb_excl) - start;
+    SW excl = 0;
+    if (t > 0) {
+      excl = look_back<R, WIN>(status_row + tid, t, a.error, a.timeout_ns, trips, polls);
+      if (FULL) st_relaxed(status_tile + tid, LW::kFlagP | (excl + my_count));
+    }
+    s.g_off[tid] = a.bases[row * a.bases_row_stride + tid] + static_cast<uint32_t>(excl) - start;
   }
   LSDRS_PHASE(4);  // thread 0's look-back
 #if LSDRS_STATS
@@ -493,7 +483,9 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
       uint32_t v = 0;
       if constexpr (kVals) v = io.vals[j];
       const uint32_t d = pass_digit<KeyOp, BYTE>(k, a);
+      if (!in_bounds(d < R, a.error, 6)) continue;
       const uint32_t g = s.g_off[d] + static_cast<uint32_t>(j);
+      if (!in_bounds(g < a.cols, a.error, 7)) continue;
       kout[g] = k;
       if constexpr (kVals) {
         if (wide)
@@ -541,6 +533,7 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   S& s = *reinterpret_cast<S*>(smem_raw);
   const int tid = threadIdx.x;
+  grid_dependency_sync();
 
   // the tile id and this pass's schedule code in one word
   if (tid == 0) {
@@ -550,9 +543,8 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
     s.abort = ld_relaxed(a.error) != kErrNone;
     s.scratch.skip_stores = 0;
   }
-  constexpr int kCnt16B = W * R * static_cast<int>(sizeof(WarpCount)) / 16;
-  static_assert((W * R * sizeof(WarpCount)) % 16 == 0, "counters are zeroed 16 bytes at a time");
-  for (int i = tid; i < kCnt16B; i += THREADS)
+  static_assert((W * R) % 4 == 0, "counters are zeroed 16 bytes at a time");
+  for (int i = tid; i < W * R / 4; i += THREADS)
     reinterpret_cast<uint4*>(&s.scratch.warp_cnt[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
 
@@ -634,8 +626,7 @@ cudaError_t launch_with_smem(K kern, unsigned grid, int threads, size_t smem, cu
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  kern<<<grid, threads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(kern, grid, threads, smem, s, a);
 }
 
 // One pass: every full tile, then each row's partial tile, in one launch.

@@ -101,6 +101,7 @@ __device__ __forceinline__ void copy_bytes(void* dst, const void* src, size_t by
 }
 
 __global__ void __launch_bounds__(kCopyThreads) finish_kernel(FinishArgs f) {
+  grid_dependency_sync();
   const uint32_t m = *f.passes_run;
   const void* ksrc = nullptr;
   const void* vsrc = nullptr;
@@ -130,8 +131,7 @@ cudaError_t launch_finish(const FinishArgs& f, cudaStream_t s) {
   const size_t cap = 4 * static_cast<size_t>(device_sm_count());
   if (grid > cap) grid = cap;
   if (grid == 0) grid = 1;
-  finish_kernel<<<static_cast<unsigned>(grid), kCopyThreads, 0, s>>>(f);
-  return cudaGetLastError();
+  return launch_kernel(finish_kernel, static_cast<unsigned>(grid), kCopyThreads, 0, s, f);
 }
 
 cudaError_t launch_timeout_probe(uint32_t* word, uint32_t* error, uint64_t timeout_ns,

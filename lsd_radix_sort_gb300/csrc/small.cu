@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(THREADS) small_sort_kernel(SmallArgs a) {
   static_assert(R <= THREADS, "one thread per digit");
   extern __shared__ __align__(16) unsigned char smem_raw[];
   S& s = *reinterpret_cast<S*>(smem_raw);
+  grid_dependency_sync();
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -59,7 +60,7 @@ __global__ void __launch_bounds__(THREADS) small_sort_kernel(SmallArgs a) {
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
       const int p = wpos + i * kWarp;
-      keys[i] = p < valid ? src[p] : T(0);
+      keys[i] = (p < valid && in_bounds(p < S::kTile, a.header, 20)) ? src[p] : T(0);
       vals[i] = VK == kValIdx ? static_cast<uint32_t>(p) : ((kVals && p < valid) ? vsrc[p] : 0u);
     }
   }
@@ -78,9 +79,10 @@ __global__ void __launch_bounds__(THREADS) small_sort_kernel(SmallArgs a) {
       const uint32_t d = wpos + i * kWarp < valid ? KeyOp::digit(keys[i], shift, mask, a.xf)
                                                   : static_cast<uint32_t>(R - 1);
       const uint32_t peers = digit_peers<BITS>(d);
-      const uint32_t before = wc[d];
+      const bool d_ok = in_bounds(d < R, a.header, 21);
+      const uint32_t before = d_ok ? wc[d] : 0u;
       __syncwarp();
-      wc[d] = before + __popc(peers);
+      if (d_ok) wc[d] = before + __popc(peers);
       __syncwarp();
       dig[i] = d;
       rank[i] = before + __popc(peers & lt);
@@ -119,7 +121,9 @@ __global__ void __launch_bounds__(THREADS) small_sort_kernel(SmallArgs a) {
     // scatter to this pass's order, then read back warp-striped
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
+      if (!in_bounds(dig[i] < R, a.header, 22)) continue;
       const uint32_t pos = s.warp_cnt[warp][dig[i]] + rank[i];
+      if (!in_bounds(pos < S::kTile, a.header, 23)) continue;
       s.stage[pos] = keys[i];
       if (kVals) s.vals[pos] = vals[i];
     }
@@ -153,8 +157,7 @@ cudaError_t launch_small_t(const SmallArgs& a, cudaStream_t s) {
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  kern<<<static_cast<unsigned>(a.rows), THREADS, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(kern, static_cast<unsigned>(a.rows), THREADS, smem, s, a);
 }
 
 // Three tile sizes: 1,024 keys (256 threads x 4), 4,096 (512 x 8) and 8,192

@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(kCountThreads) tile_count_kernel(TileCountArgs
   constexpr int R = 1 << BITS;
   constexpr int W = kCountThreads / kWarp;
   __shared__ uint32_t cnt[W][R];
+  grid_dependency_sync();
   const int tid = threadIdx.x;
   for (int i = tid; i < W * R; i += kCountThreads) (&cnt[0][0])[i] = 0;
   __syncthreads();
@@ -50,6 +51,7 @@ __global__ void __launch_bounds__(kCountThreads) tile_count_kernel(TileCountArgs
 
 template <int R>
 __global__ void __launch_bounds__(R < kWarp ? kWarp : R) tile_scan_kernel(TileCountArgs a) {
+  grid_dependency_sync();
   const int d = threadIdx.x;
   if (d >= R) return;
   const int64_t row = blockIdx.x;
@@ -67,11 +69,10 @@ __global__ void __launch_bounds__(R < kWarp ? kWarp : R) tile_scan_kernel(TileCo
 cudaError_t launch_tile_counts_f16(const TileCountArgs& a, cudaStream_t s) {
   const int64_t tiles = a.rows * a.tiles_per_row;
   if (tiles == 0) return cudaSuccess;
-  tile_count_kernel<KeyF16Bits, 8><<<static_cast<unsigned>(tiles), kCountThreads, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_kernel(tile_count_kernel<KeyF16Bits, 8>, static_cast<unsigned>(tiles),
+                                kCountThreads, 0, s, a);
   if (e != cudaSuccess) return e;
-  tile_scan_kernel<256><<<static_cast<unsigned>(a.rows), 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_kernel(tile_scan_kernel<256>, static_cast<unsigned>(a.rows), 256, 0, s, a);
 }
 
 }  // namespace lsdrs
