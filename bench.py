@@ -602,7 +602,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--n", dest="n_log2", type=int, default=28)
     ap.add_argument("--ref-log2", type=int, default=24)
-    ap.add_argument("--cpu-log2", type=int, default=26)
+    ap.add_argument("--cpu-log2", type=int, default=28)
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-distributions", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")

@@ -195,8 +195,11 @@ rs_status radix_segmented_sort_temp_bytes(int64_t rows, int64_t cols, size_t* by
 /* Row-wise stable sort of 16-bit floats along the last dimension, returning
  * the sorted values and their int64 column indices (FlagTree PR #1084: a
  * radix `sort` of fp16/bf16 rows with a descending flag folded into an
- * order-preserving key, two 8-bit passes, int32 indices inside and int64 on
- * the way out).
+ * order-preserving key, two 8-bit passes, compact indices inside and int64
+ * on the way out).  Between the passes a row of at most 65,536 columns
+ * carries each key and its column in one 32-bit word (key << 16 | column);
+ * longer rows, and the pass-skipping and precomputed-offset modes, carry an
+ * int32 index array beside 16-bit keys.  The results are the same.
  *   in        (device) rows*cols 16-bit patterns, row-major, contiguous
  *   vals_out  (device) rows*cols patterns: each row sorted
  *   idx_out   (device) rows*cols int64: idx_out[r][j] is the column of in[r]

@@ -320,6 +320,16 @@ rs_status run_sort(Plan p, const void* keys_in, void* keys_out, const void* vals
   // look-back; that mode keeps the static schedule (every pass runs)
   const bool precomputed = p.val == kValIdx && opt.tile_offsets;
   const bool dynamic = !precomputed && opt.pass_skipping;
+  // Row-wise sorts of rows of at most 65,536 columns on the static schedule
+  // carry each key's column in the low half of a 32-bit word between the
+  // passes (the packed words use the payload ping-pong buffer), so each pass
+  // stages one word per key; their tile is the packed kernel's.
+  const bool packed = p.val == kValIdx && !precomputed && !dynamic && p.cols <= kPackMaxCols;
+  if (packed) {
+    p.tile = kShapeF16Packed.tile();
+    p.tiles_per_row = cdiv(p.cols, p.tile);
+    p.tiles = p.rows * p.tiles_per_row;  // fewer than planned: the look-back arrays fit
+  }
   configure(&p);
   rs_status st = run_front(p, keys_in, xf, temp, nullptr, nullptr, in_place, dynamic, s);
   if (st != RS_OK) return st;
@@ -333,7 +343,8 @@ rs_status run_sort(Plan p, const void* keys_in, void* keys_out, const void* vals
   const uint32_t* bases = reinterpret_cast<const uint32_t*>(at(temp, p.off_bases));
   SweepArgs a{};
   a.keys[kBufIn] = keys_in;
-  a.keys[kBufAlt] = alt_keys;
+  a.keys[kBufAlt] = packed ? alt_vals : alt_keys;
+  a.packed = packed ? 1 : 0;
   a.keys[kBufOut] = keys_out;
   a.vals[kBufIn] = p.val == kValU32 ? vals_in : nullptr;
   a.vals[kBufAlt] = p.val == kValNone ? nullptr : alt_vals;
@@ -359,7 +370,10 @@ rs_status run_sort(Plan p, const void* keys_in, void* keys_out, const void* vals
     const uint32_t src = a.code & kCodeSrc, dst = (a.code & kCodeDst) >> 2;
     a.pass_keys_in = a.keys[src];
     a.pass_keys_out = const_cast<void*>(a.keys[dst]);
-    if (p.val == kValIdx) {
+    if (packed) {
+      a.pass_vals_in = nullptr;  // the columns travel inside the key words
+      a.pass_vals_out = last ? vals_out : nullptr;
+    } else if (p.val == kValIdx) {
       a.pass_vals_in = q == 0 ? nullptr : alt_vals;
       a.pass_vals_out = last ? vals_out : alt_vals;
     } else {

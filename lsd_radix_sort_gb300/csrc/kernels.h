@@ -19,7 +19,12 @@ struct KeyXform {
 // Payload carried with the keys: none, a u32 array, or a column index that
 // is generated in the first pass, kept as int32 and widened to int64 by the
 // last pass.
-enum ValKind { kValNone = 0, kValU32 = 1, kValIdx = 2 };
+// kValPack16: row-wise 16-bit sorts of rows of at most 65,536 columns whose
+// column index rides in the low half of a packed 32-bit word (KeyF16Packed):
+// the first pass reads 16-bit keys and generates the index, the last writes
+// the values and int64 indices, the passes between move packed words.
+enum ValKind { kValNone = 0, kValU32 = 1, kValIdx = 2, kValPack16 = 3 };
+constexpr int64_t kPackMaxCols = 65536;
 
 // Threads per CTA and keys per thread of the onesweep kernel, per
 // (key, payload) combination.  The tile is THREADS * ITEMS keys.
@@ -74,15 +79,25 @@ struct SweepShape {
 #ifndef LSDRS_F16_W
 #define LSDRS_F16_W 4
 #endif
+#ifndef LSDRS_F16P_T
+#define LSDRS_F16P_T 256
+#define LSDRS_F16P_I 32
+#define LSDRS_F16P_B 4
+#endif
+#ifndef LSDRS_F16P_W
+#define LSDRS_F16P_W 4
+#endif
 constexpr SweepShape kShapeU32Keys{LSDRS_U32K_T, LSDRS_U32K_I, LSDRS_U32K_B, LSDRS_U32K_W};
 constexpr SweepShape kShapeU32Pairs{LSDRS_U32P_T, LSDRS_U32P_I, LSDRS_U32P_B, LSDRS_U32P_W};
 constexpr SweepShape kShapeU64Keys{LSDRS_U64K_T, LSDRS_U64K_I, LSDRS_U64K_B, LSDRS_U64K_W};
 constexpr SweepShape kShapeU64Pairs{LSDRS_U64P_T, LSDRS_U64P_I, LSDRS_U64P_B, LSDRS_U64P_W};
 constexpr SweepShape kShapeF16Idx{LSDRS_F16_T, LSDRS_F16_I, LSDRS_F16_B, LSDRS_F16_W};
+constexpr SweepShape kShapeF16Packed{LSDRS_F16P_T, LSDRS_F16P_I, LSDRS_F16P_B, LSDRS_F16P_W};
 constexpr SweepShape sweep_shape(KeyKind k, ValKind v) {
   return (k == kKeyU32 || k == kKeyX32) ? (v == kValNone ? kShapeU32Keys : kShapeU32Pairs)
        : (k == kKeyU64 || k == kKeyX64) ? (v == kValNone ? kShapeU64Keys : kShapeU64Pairs)
-                      : kShapeF16Idx;
+       : v == kValPack16                ? kShapeF16Packed
+                                        : kShapeF16Idx;
 }
 
 constexpr int kHistThreads = 1024;
@@ -194,6 +209,7 @@ struct SweepArgs {
                            // ids below rows * full_per_row are full tiles, then one
                            // partial tile per row when cols is not a whole number of tiles
   int wide;                // 64-bit look-back words (flat sorts of 2^30 keys or more)
+  int packed;              // row-wise: keys and columns packed in 32-bit words (kValPack16)
   int dynamic;             // the schedule comes from K-SCAN (pass skipping on)
   uint32_t code;           // otherwise: this pass's code, from the host, and
   const void* pass_keys_in;   // the buffers and look-back words it selects

@@ -119,4 +119,24 @@ struct KeyF16Bits {
   }
 };
 
+// A 16-bit float key packed with its 16-bit column index into one word,
+// (bits << 16) | column: the form a row of at most 65,536 columns takes
+// between the two passes of a row-wise sort, so that each pass moves and
+// stages one 32-bit word per key.  The digits are those of T(bits).
+struct KeyF16Packed {
+  using T = uint32_t;
+  static constexpr int kBits = 16;
+  __device__ __forceinline__ static uint32_t encode(T w, const KeyXform& x) {
+    return KeyF16Bits::encode(static_cast<uint16_t>(w >> 16), x);
+  }
+  __device__ __forceinline__ static uint32_t digit(T w, int shift, uint32_t mask,
+                                                   const KeyXform& x) {
+    return (encode(w, x) >> shift) & mask;
+  }
+  __device__ __forceinline__ static uint32_t digit_byte(T w, uint32_t sel, bool,
+                                                        const KeyXform& x) {
+    return __byte_perm(encode(w, x), 0u, sel);
+  }
+};
+
 }  // namespace lsdrs

@@ -298,7 +298,8 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   constexpr int W = THREADS / kWarp;
   constexpr int TILE = THREADS * ITEMS;
   constexpr int WKEYS = kWarp * ITEMS;
-  constexpr bool kVals = VK != kValNone;
+  constexpr bool kVals = VK == kValU32 || VK == kValIdx;  // a payload array travels
+  constexpr bool kPack = VK == kValPack16;                // column index inside the key word
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -312,13 +313,26 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
 #endif
 
   T keys[ITEMS];
+  if (kPack && PassBufs<DYN>{DYN ? s.code : a.code, a}.first()) {
+    // the row's 16-bit keys, each packed with its column
+    const uint16_t* src16 = reinterpret_cast<const uint16_t*>(io.key_src);
 #pragma unroll
-  for (int i = 0; i < ITEMS; ++i)
-    keys[i] = ((FULL || wpos + i * kWarp < valid) &&
-               in_bounds(wpos + i * kWarp < valid && tile_begin + wpos + i * kWarp < a.cols,
-                         a.error, 1))
-                  ? io.key_src[wpos + i * kWarp]
-                  : T(0);
+    for (int i = 0; i < ITEMS; ++i) {
+      const int p = wpos + i * kWarp;
+      keys[i] = ((FULL || p < valid) &&
+                 in_bounds(p < valid && tile_begin + p < a.cols, a.error, 1))
+                    ? (static_cast<uint32_t>(src16[p]) << 16) | static_cast<uint32_t>(tile_begin + p)
+                    : T(0);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i)
+      keys[i] = ((FULL || wpos + i * kWarp < valid) &&
+                 in_bounds(wpos + i * kWarp < valid && tile_begin + wpos + i * kWarp < a.cols,
+                           a.error, 1))
+                    ? io.key_src[wpos + i * kWarp]
+                    : T(0);
+  }
 
   // ---- 3. rank within the warp ------------------------------------------
   // The rank of item i among the warp's keys of its digit (below
@@ -475,6 +489,24 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   uint32_t* vout32 = static_cast<uint32_t*>(pb.template vals_out<VK>()) + row_base;
   int64_t* vout64 = static_cast<int64_t*>(pb.template vals_out<VK>()) + row_base;
   const bool wide = VK == kValIdx && pb.last();
+  if (kPack && pb.last()) {
+    // the packed words leave as the row's values and their int64 columns
+    uint16_t* v16 = static_cast<uint16_t*>(pb.keys_out()) + row_base;
+#pragma unroll
+    for (int i = 0; i < ITEMS; ++i) {
+      const int j = i * THREADS + tid;
+      if (FULL || j < valid) {
+        const T k = io.stage_keys[j];
+        const uint32_t d = pass_digit<KeyOp, BYTE>(k, a);
+        if (!in_bounds(d < R, a.error, 6)) continue;
+        const uint32_t g = s.g_off[d] + static_cast<uint32_t>(j);
+        if (!in_bounds(g < a.cols, a.error, 7)) continue;
+        v16[g] = static_cast<uint16_t>(k >> 16);
+        vout64[g] = static_cast<int64_t>(k & 0xFFFFu);
+      }
+    }
+    return;
+  }
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
     const int j = i * THREADS + tid;
@@ -503,7 +535,7 @@ template <class KeyOp, int BITS, int VK, int THREADS, int ITEMS>
 struct SweepSmem {
   using T = typename KeyOp::T;
   static constexpr int kTile = THREADS * ITEMS;
-  static constexpr bool kVals = VK != kValNone;
+  static constexpr bool kVals = VK == kValU32 || VK == kValIdx;
   alignas(128) T stage[kTile];                    // keys in tile-sorted order
   alignas(128) uint32_t vals[kVals ? kTile : 4];  // payloads in, then their stage
   TileScratch<THREADS / kWarp, (1 << BITS)> scratch;
@@ -573,6 +605,8 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
   SW* status_row = static_cast<SW*>(pb.status()) + (row * a.full_per_row) * R;
   TileIo<KeyOp> io;
   io.key_src = static_cast<const T*>(pb.keys_in()) + off;
+  if (VK == kValPack16 && pb.first())  // 16-bit keys: offset in 16-bit units
+    io.key_src = reinterpret_cast<const T*>(static_cast<const uint16_t*>(pb.keys_in()) + off);
   io.stage_keys = s.stage;
   io.vals = s.vals;
   io.val_bar = nullptr;
@@ -580,7 +614,7 @@ __device__ __forceinline__ void onesweep_body(const SweepArgs& a) {
   if (s.abort) {  // an earlier tile failed: release successors and stop
     if (full && !PRE && tid < R) st_relaxed(status_row + t * R + tid, LookbackWord<SW>::kFlagP);
   } else {
-    if (VK != kValNone && pb.template vals_in<VK>() != nullptr) {
+    if ((VK == kValU32 || VK == kValIdx) && pb.template vals_in<VK>() != nullptr) {
       // Payloads are not needed before the staging step: a full tile with an
       // aligned source gets them by one bulk copy issued now (the tile's
       // first block-wide barrier orders the barrier's initialisation before
