@@ -13,6 +13,8 @@
 // and scans (DSA CUDA from First Principles, section 13.1: the base of digit
 // d is the exclusive prefix sum of the counts of the digits below it).
 #pragma once
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "keys.cuh"
@@ -23,12 +25,25 @@ namespace lsdrs {
 // columns every lane of a warp owns its own column and bank, so a warp's 32
 // increments never collide, whatever the digits are (constant input included).
 // 16 columns when 32 would not fit in shared memory (64-bit keys, 8-bit digits).
+// Row-wise 16-bit sorts count each row in its own CTA (a row of a few tens
+// of thousands of keys): threads and counter columns for those (build-time).
+#ifndef LSDRS_HIST_F16_THREADS
+#define LSDRS_HIST_F16_THREADS 512
+#endif
+#ifndef LSDRS_HIST_F16_COLS
+#define LSDRS_HIST_F16_COLS 16
+#endif
+
 template <class KeyOp, int BITS>
 struct HistCfg {
+  static constexpr bool kRows = std::is_same<KeyOp, KeyF16Bits>::value;
+  static constexpr int kThreads = kRows ? LSDRS_HIST_F16_THREADS : kHistThreads;
   static constexpr int kRadix = 1 << BITS;
   static constexpr int kMaxPasses = (KeyOp::kBits + BITS - 1) / BITS;
   static constexpr int kCols =
-      static_cast<size_t>(kMaxPasses) * kRadix * 32 * sizeof(uint32_t) <= 128 * 1024 ? 32 : 16;
+      kRows ? LSDRS_HIST_F16_COLS
+            : (static_cast<size_t>(kMaxPasses) * kRadix * 32 * sizeof(uint32_t) <= 128 * 1024 ? 32
+                                                                                             : 16);
   static constexpr int kVec = 16 / sizeof(typename KeyOp::T);
   static constexpr int kUnroll = 4;
   static size_t smem_bytes(int passes) {
@@ -120,12 +135,12 @@ __device__ __forceinline__ void count_range(const typename KeyOp::T* base, int64
     c.add(base[body_end + tid]);
   const uint4* vp = reinterpret_cast<const uint4*>(base + body_begin);
   int64_t v = tid;
-  for (; v + (U - 1) * kHistThreads < nvec; v += U * kHistThreads) {
+  for (; v + (U - 1) * Cfg::kThreads < nvec; v += U * Cfg::kThreads) {
     uint4 buf[U];
 #pragma unroll
     for (int u = 0; u < U; ++u)
-      buf[u] = in_bounds(body_begin + (v + u * kHistThreads + 1) * V <= cols, c.hdr, 15)
-                   ? __ldcs(vp + v + u * kHistThreads)
+      buf[u] = in_bounds(body_begin + (v + u * Cfg::kThreads + 1) * V <= cols, c.hdr, 15)
+                   ? __ldcs(vp + v + u * Cfg::kThreads)
                    : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -134,7 +149,7 @@ __device__ __forceinline__ void count_range(const typename KeyOp::T* base, int64
       for (int e = 0; e < V; ++e) c.add(ks[e]);
     }
   }
-  for (; v < nvec; v += kHistThreads) {
+  for (; v < nvec; v += Cfg::kThreads) {
     if (!in_bounds(body_begin + (v + 1) * V <= cols, c.hdr, 16)) continue;
     uint4 b = __ldcs(vp + v);
     const T* ks = reinterpret_cast<const T*>(&b);
@@ -144,7 +159,8 @@ __device__ __forceinline__ void count_range(const typename KeyOp::T* base, int64
 }
 
 template <class KeyOp, int BITS>
-__global__ void __launch_bounds__(kHistThreads, 1) upfront_hist_kernel(HistArgs a) {
+__global__ void __launch_bounds__(HistCfg<KeyOp, BITS>::kThreads, 1)
+    upfront_hist_kernel(HistArgs a) {
   using T = typename KeyOp::T;
   using Cfg = HistCfg<KeyOp, BITS>;
   constexpr int R = Cfg::kRadix;
@@ -154,12 +170,12 @@ __global__ void __launch_bounds__(kHistThreads, 1) upfront_hist_kernel(HistArgs 
 
   const int tid = threadIdx.x;
   const int nb = a.passes * R;
-  for (int i = tid; i < nb * C; i += kHistThreads) cnt[i] = 0;
+  for (int i = tid; i < nb * C; i += Cfg::kThreads) cnt[i] = 0;
 
   // Zero the look-back words and counters the sweeps start from.
   {
-    const size_t stride = static_cast<size_t>(gridDim.x) * kHistThreads;
-    for (size_t i = static_cast<size_t>(blockIdx.x) * kHistThreads + tid; i < a.zero_words;
+    const size_t stride = static_cast<size_t>(gridDim.x) * Cfg::kThreads;
+    for (size_t i = static_cast<size_t>(blockIdx.x) * Cfg::kThreads + tid; i < a.zero_words;
          i += stride)
       if (i < kHdrViolations || i >= kHdrViolations + 2) a.zero_ptr[i] = 0;
   }
@@ -191,7 +207,7 @@ __global__ void __launch_bounds__(kHistThreads, 1) upfront_hist_kernel(HistArgs 
   __syncthreads();
 
   uint32_t* slot = a.slots + static_cast<int64_t>(blockIdx.x) * nb;
-  for (int b = tid; b < nb; b += kHistThreads) {
+  for (int b = tid; b < nb; b += Cfg::kThreads) {
     uint32_t s = 0;
 #pragma unroll
     for (int k = 0; k < C; ++k) s += cnt[b * C + (k + b) % C];
@@ -209,7 +225,7 @@ cudaError_t launch_hist_t(const HistArgs& a, int grid, cudaStream_t s) {
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  return launch_kernel(kern, grid, kHistThreads, smem, s, a);
+  return launch_kernel(kern, grid, Cfg::kThreads, smem, s, a);
 }
 
 template <class KeyOp>
