@@ -2,12 +2,14 @@
 
     python -m lsd_radix_sort_gb300.profile_case CASE [--log2 N] [--bits B]
                                                 [--sorts K] [--warmup W]
+                                                [--rows R] [--cols C]
 
 CASE is one of
   pairs_u32   N u32 keys + u32 index payload (uniform 32-bit keys, seed 0)
   keys_u32    N u32 keys only (uniform, seed 0)
   pairs_u64   N u64 keys + u32 index payload (uniform 64-bit keys, seed 0)
-  rows_f16    (1024, 65536) fp16 rows (the standard-normal mix), ascending
+  rows_f16    (R, C) fp16 rows (the standard-normal mix), ascending; by
+              default (1024, 65536)
   rows_bf16   the same rows in bf16
 
 Each sort is timed with CUDA events around every kernel the library enqueues
@@ -33,6 +35,8 @@ def main():
     ap.add_argument("--end-bit", type=int, default=None)
     ap.add_argument("--sorts", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=2)
+    ap.add_argument("--rows", type=int, default=1024, help="rows of the row-wise cases")
+    ap.add_argument("--cols", type=int, default=65536, help="columns of the row-wise cases")
     args = ap.parse_args()
 
     import torch
@@ -75,7 +79,7 @@ def main():
         units = n
     else:
         kind = "f16" if args.case == "rows_f16" else "bf16"
-        rows, cols = 1024, 65536
+        rows, cols = args.rows, args.cols
         x = torch.from_numpy(workloads.rows16(rows, cols, kind, 0).view(np.int16)).to(dev)
         x = x.view(torch.float16 if kind == "f16" else torch.bfloat16)
         v = torch.empty_like(x)
