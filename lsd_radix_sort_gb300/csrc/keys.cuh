@@ -120,22 +120,35 @@ struct KeyF16Bits {
 };
 
 // A 16-bit float key packed with its 16-bit column index into one word,
-// (bits << 16) | column: the form a row of at most 65,536 columns takes
+// (T(bits) << 16) | column: the form a row of at most 65,536 columns takes
 // between the two passes of a row-wise sort, so that each pass moves and
-// stages one 32-bit word per key.  The digits are those of T(bits).
+// stages one 32-bit word per key.  The order-preserving transform is applied
+// once, when the word is made (pack), and undone once, when the last pass
+// writes the value out (bits): a digit is then one byte permute.
 struct KeyF16Packed {
   using T = uint32_t;
   static constexpr int kBits = 16;
-  __device__ __forceinline__ static uint32_t encode(T w, const KeyXform& x) {
-    return KeyF16Bits::encode(static_cast<uint16_t>(w >> 16), x);
+  __device__ __forceinline__ static uint32_t pack(uint16_t bits, uint32_t col,
+                                                  const KeyXform& x) {
+    return (KeyF16Bits::encode(bits, x) << 16) | col;
   }
+  // The 16-bit pattern of the word's key: T is u ^ pos for u >= 0 and
+  // u ^ neg for u < 0, and the sign bit of T(u) ^ pos is set exactly for the
+  // latter, so the key's sign is read back from T.
+  __device__ __forceinline__ static uint16_t bits(T w, const KeyXform& x) {
+    const uint32_t t = w >> 16;
+    const uint32_t pos = static_cast<uint32_t>(x.pos), neg = static_cast<uint32_t>(x.neg);
+    return static_cast<uint16_t>(t ^ (((t ^ pos) & 0x8000u) ? neg : pos));
+  }
+  __device__ __forceinline__ static uint32_t encode(T w, const KeyXform&) { return w >> 16; }
   __device__ __forceinline__ static uint32_t digit(T w, int shift, uint32_t mask,
-                                                   const KeyXform& x) {
-    return (encode(w, x) >> shift) & mask;
+                                                   const KeyXform&) {
+    return (w >> (16 + shift)) & mask;
   }
+  // sel selects byte b (0 or 1) of T: bytes 2 and 3 of the word
   __device__ __forceinline__ static uint32_t digit_byte(T w, uint32_t sel, bool,
-                                                        const KeyXform& x) {
-    return __byte_perm(encode(w, x), 0u, sel);
+                                                        const KeyXform&) {
+    return __byte_perm(w, 0u, sel + 2u);
   }
 };
 

@@ -314,14 +314,14 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
 
   T keys[ITEMS];
   if (kPack && PassBufs<DYN>{DYN ? s.code : a.code, a}.first()) {
-    // the row's 16-bit keys, each packed with its column
+    // the row's 16-bit keys, transformed and packed with their columns
     const uint16_t* src16 = reinterpret_cast<const uint16_t*>(io.key_src);
 #pragma unroll
     for (int i = 0; i < ITEMS; ++i) {
       const int p = wpos + i * kWarp;
       keys[i] = ((FULL || p < valid) &&
                  in_bounds(p < valid && tile_begin + p < a.cols, a.error, 1))
-                    ? (static_cast<uint32_t>(src16[p]) << 16) | static_cast<uint32_t>(tile_begin + p)
+                    ? KeyF16Packed::pack(src16[p], static_cast<uint32_t>(tile_begin + p), a.xf)
                     : T(0);
     }
   } else {
@@ -501,7 +501,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
         if (!in_bounds(d < R, a.error, 6)) continue;
         const uint32_t g = s.g_off[d] + static_cast<uint32_t>(j);
         if (!in_bounds(g < a.cols, a.error, 7)) continue;
-        v16[g] = static_cast<uint16_t>(k >> 16);
+        v16[g] = KeyF16Packed::bits(k, a.xf);
         vout64[g] = static_cast<int64_t>(k & 0xFFFFu);
       }
     }
