@@ -213,10 +213,16 @@ rs_status run_front(const Plan& p, const void* keys, const KeyXform& xf, void* t
   h.zero_words = (p.off_status1) / 4;  // header + status0
   const int64_t hgrid = p.rows * p.chunks_per_row;
   const uint64_t n = static_cast<uint64_t>(p.rows) * p.cols;
+  // 16-bit rows counted one CTA per row, static schedule: K-HIST scans
+  h.fused_scan = p.key == kKeyF16 && p.bits == 8 && p.chunks_per_row == 1 && !dynamic;
+  h.bases = reinterpret_cast<uint32_t*>(at(temp, p.off_bases));
+  h.hist_out = hist_out;
+  h.bases_out = bases_out;
   cudaError_t e = timed_launch(0, n, s, [&](int*) {
     return launch_hist(p.key, p.bits, h, static_cast<int>(hgrid), s);
   });
   if (e != cudaSuccess) return RS_ERR_CUDA;
+  if (h.fused_scan) return RS_OK;
   ScanArgs c{};
   c.slots = h.slots;
   c.rows = p.rows;

@@ -31,7 +31,13 @@ namespace lsdrs {
 #define LSDRS_HIST_F16_THREADS 512
 #endif
 #ifndef LSDRS_HIST_F16_COLS
-#define LSDRS_HIST_F16_COLS 16
+#define LSDRS_HIST_F16_COLS 32
+#endif
+#ifndef LSDRS_HIST_F16_UNROLL
+#define LSDRS_HIST_F16_UNROLL 4
+#endif
+#ifndef LSDRS_HIST_F16_MINB
+#define LSDRS_HIST_F16_MINB 3
 #endif
 
 template <class KeyOp, int BITS>
@@ -45,7 +51,8 @@ struct HistCfg {
             : (static_cast<size_t>(kMaxPasses) * kRadix * 32 * sizeof(uint32_t) <= 128 * 1024 ? 32
                                                                                              : 16);
   static constexpr int kVec = 16 / sizeof(typename KeyOp::T);
-  static constexpr int kUnroll = 4;
+  static constexpr int kUnroll = kRows ? LSDRS_HIST_F16_UNROLL : 4;
+  static constexpr int kMinBlocks = kRows ? LSDRS_HIST_F16_MINB : 1;
   static size_t smem_bytes(int passes) {
     return static_cast<size_t>(passes) * kRadix * kCols * sizeof(uint32_t);
   }
@@ -159,7 +166,7 @@ __device__ __forceinline__ void count_range(const typename KeyOp::T* base, int64
 }
 
 template <class KeyOp, int BITS>
-__global__ void __launch_bounds__(HistCfg<KeyOp, BITS>::kThreads, 1)
+__global__ void __launch_bounds__(HistCfg<KeyOp, BITS>::kThreads, HistCfg<KeyOp, BITS>::kMinBlocks)
     upfront_hist_kernel(HistArgs a) {
   using T = typename KeyOp::T;
   using Cfg = HistCfg<KeyOp, BITS>;
@@ -205,6 +212,41 @@ __global__ void __launch_bounds__(HistCfg<KeyOp, BITS>::kThreads, 1)
     }
   }
   __syncthreads();
+
+  if constexpr (Cfg::kRows && BITS == 8 && Cfg::kThreads % R == 0) {
+    if (a.fused_scan && nb <= Cfg::kThreads) {
+      // The row's totals (one CTA per row: the CTA's counts) and their
+      // exclusive scan over the digits of each pass: thread t holds digit
+      // t % R of pass t / R, and the R threads of a pass are whole warps.
+      const int lane = tid & 31, warp = tid >> 5;
+      const int p = tid / R, d = tid % R;
+      uint32_t total = 0;
+      if (tid < nb) {
+#pragma unroll
+        for (int k = 0; k < C; ++k) total += cnt[tid * C + (k + tid) % C];
+      }
+      uint32_t incl = total;
+#pragma unroll
+      for (int o = 1; o < kWarp; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+      }
+      __shared__ uint32_t warp_sums[Cfg::kThreads / kWarp];
+      if (lane == kWarp - 1) warp_sums[warp] = incl;
+      __syncthreads();
+      uint32_t excl = incl - total;
+      for (int w = p * (R / kWarp); w < warp; ++w) excl += warp_sums[w];
+      if (tid < nb) {
+        const int64_t o = (row * a.passes + p) * R + d;
+        a.bases[o] = excl;
+        if (a.hist_out) a.hist_out[o] = total;
+        if (a.bases_out) a.bases_out[o] = excl;
+      }
+      // every pass runs (this CTA zeroed the header word above)
+      if (blockIdx.x == 0 && tid == 0) a.zero_ptr[kHdrPassesRun] = static_cast<uint32_t>(a.passes);
+      return;
+    }
+  }
 
   uint32_t* slot = a.slots + static_cast<int64_t>(blockIdx.x) * nb;
   for (int b = tid; b < nb; b += Cfg::kThreads) {

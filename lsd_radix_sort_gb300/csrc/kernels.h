@@ -126,6 +126,13 @@ struct HistArgs {
   uint32_t* slots;         // [rows][chunks_per_row][passes][radix] counts
   uint32_t* zero_ptr;      // words zeroed by the grid before any sweep
   size_t zero_words;
+  // Row-wise 16-bit sorts counted one CTA per row on the static schedule:
+  // the CTA scans its own counts into `bases` (and the optional copies), so
+  // no K-SCAN runs.  `zero_ptr` is the scratch header.
+  int fused_scan;
+  uint32_t* bases;         // [rows][passes][radix] exclusive scans
+  uint32_t* hist_out;      // optional [rows][passes][radix] totals
+  uint32_t* bases_out;     // optional [rows][passes][radix] exclusive scans
 };
 
 // Scratch header (u32 words): the device error word, one tile counter per
