@@ -334,6 +334,15 @@ rs_status radix_sort_pairs_u32_noalloc(const uint32_t* keys_in, uint32_t* keys_o
  * nothing. */
 rs_status radix_sort_pairs_u32_noalloc_status(void* stream);
 
+/* Verification of the status path above (no sort): runs the look-back's
+ * bounded wait on a word of the no-allocation array that nothing sets, with
+ * the given limit (1 ns .. 60 s), so that it records RS_ERR_LOOKBACK_TIMEOUT
+ * in the array's device-side status word, exactly where a timed-out sort of
+ * radix_sort_pairs_u32_noalloc records it; the next such sort clears it.
+ * Synchronises `stream`; writes the probe's own reading of the word to
+ * *result.  Allocates nothing. */
+rs_status rs_noalloc_timeout_probe(uint64_t timeout_ns, void* stream, rs_status* result);
+
 #ifdef __cplusplus
 }
 #endif

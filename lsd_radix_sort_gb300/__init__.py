@@ -29,7 +29,7 @@ __all__ = [
     "radix_sort_pairs", "segmented_sort", "segmented_temp_bytes", "upfront_histograms",
     "device_status", "passes_run", "SMALL_SORT_MAX_KEYS", "copy_probe",
     "lookback_timeout_probe", "profile_enable", "profile_read", "launch_count_reset",
-    "noalloc_status", "EXPORTED_SYMBOLS", "RS_MAX_KEYS", "RS_MAX_ROW_KEYS", "checked_build",
+    "noalloc_status", "noalloc_timeout_probe", "EXPORTED_SYMBOLS", "RS_MAX_KEYS", "RS_MAX_ROW_KEYS", "checked_build",
     "BoundsViolation",
 ]
 
@@ -55,7 +55,7 @@ EXPORTED_SYMBOLS = (
     "radix_sort_device_status", "rs_status_string", "rs_lookback_timeout_probe",
     "rs_copy_probe", "rs_profile_enable", "rs_profile_read", "rs_launch_count_reset",
     "radix_sort_pairs_u32_noalloc", "radix_sort_pairs_u32_noalloc_status",
-    "radix_sort_keys_typed", "radix_sort_pairs_typed", "radix_sort_passes_run",
+    "rs_noalloc_timeout_probe", "radix_sort_keys_typed", "radix_sort_pairs_typed", "radix_sort_passes_run",
     "rs_checked_build", "radix_sort_checked_violations",
 )
 
@@ -129,6 +129,7 @@ def load_library() -> ctypes.CDLL:
             "rs_profile_enable": [i],
             "radix_sort_pairs_u32_noalloc": [P, P, P, P, sz, i, i, i, P],
             "radix_sort_pairs_u32_noalloc_status": [P],
+            "rs_noalloc_timeout_probe": [u64, P, P],
             "radix_sort_keys_typed": [i, i, P, P, sz, i, i, i, P, sz, P, P],
             "radix_sort_passes_run": [P, P, P],
             "radix_sort_pairs_typed": [i, i, P, P, P, P, sz, i, i, i, P, sz, P, P],
@@ -486,3 +487,13 @@ def noalloc_status(stream=None) -> int:
     """Synchronise and return the device-side status of the last no-allocation
     sort enqueued on the current device (radix_sort_pairs_u32_noalloc_status)."""
     return int(load_library().radix_sort_pairs_u32_noalloc_status(_stream_ptr(stream)))
+
+
+def noalloc_timeout_probe(timeout_ns: int, stream=None) -> int:
+    """Run the bounded look-back wait on a word of the no-allocation array
+    that nothing sets (rs_noalloc_timeout_probe); return its status."""
+    res = ctypes.c_int(-1)
+    _check(load_library().rs_noalloc_timeout_probe(int(timeout_ns), _stream_ptr(stream),
+                                                   ctypes.byref(res)),
+           "rs_noalloc_timeout_probe")
+    return res.value

@@ -768,6 +768,29 @@ extern "C" rs_status radix_sort_pairs_u32_noalloc(const uint32_t* keys_in, uint3
                   kNoAllocScratchBytes, Options{}, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" rs_status rs_noalloc_timeout_probe(uint64_t timeout_ns, void* stream,
+                                             rs_status* result) {
+  if (!result || timeout_ns == 0 || timeout_ns > kMaxTimeoutNs) return RS_ERR_INVALID;
+  void* scratch = nullptr;
+  rs_status st = noalloc_scratch(&scratch);
+  if (st != RS_OK) return st;
+  uint32_t* hdr = static_cast<uint32_t*>(scratch);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(hdr + kHdrProbeWord, 0, 4, s) != cudaSuccess ||
+      cudaMemsetAsync(hdr + kHdrError, 0, 4, s) != cudaSuccess)
+    return RS_ERR_CUDA;
+  cudaError_t e = timed_launch(4, 1, s, [&](int*) {
+    return launch_timeout_probe(hdr + kHdrProbeWord, hdr + kHdrError, timeout_ns, s);
+  });
+  if (e != cudaSuccess) return RS_ERR_CUDA;
+  uint32_t err = 0;
+  if (cudaMemcpyAsync(&err, hdr + kHdrError, 4, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return RS_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return RS_ERR_CUDA;
+  *result = err == kErrNone ? RS_OK : static_cast<rs_status>(err);
+  return RS_OK;
+}
+
 extern "C" rs_status radix_sort_pairs_u32_noalloc_status(void* stream) {
   void* scratch = nullptr;
   rs_status st = noalloc_scratch(&scratch);

@@ -142,6 +142,7 @@ constexpr int kHdrTileCounter = 1;     // + pass
 constexpr int kHdrScanDone = 65;       // K-SCAN CTAs finished
 constexpr int kHdrPassesRun = 66;      // passes the schedule executes
 constexpr int kHdrNontrivial = 128;    // + pass: some row has two digits in it
+constexpr int kHdrProbeWord = 96;      // a word nothing sets, for the timeout probe
 constexpr int kMaxPasses = 64;
 // Words kHdrViolations.. (common.cuh): bounds-checked builds' failed index
 // tests; K-HIST's zeroing skips them, radix_sort_checked_violations reads

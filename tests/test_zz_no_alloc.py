@@ -6,7 +6,9 @@ no-allocation entry point keeps its scratch in a fixed array of the
 library's device code instead; it must give exactly what the ordinary entry
 point gives (and what the oracle gives), call after call, although every
 call reuses (and finds dirty) the same array, and its device-side status
-must be readable through its own status call.
+must be readable through its own status call: a look-back wait that runs
+out (the probe runs the sort's bounded wait on a word of the array that
+nothing sets) is reported there, and the next sort clears it.
 """
 import ctypes
 
@@ -58,3 +60,22 @@ def test_no_alloc_rejects_beyond_its_maximum(rs):
     d = torch.empty(4, dtype=torch.int32, device="cuda")
     assert call_noalloc(lib, d, d, d, d, MAX_KEYS + 1) == rs.RS_ERR_INVALID
     assert call_noalloc(lib, d, d, d, d, 0) == rs.RS_OK
+
+
+def test_no_alloc_status_reports_a_timed_out_wait(rs):
+    lib = rs.load_library()
+    n = 50_000
+    keys, vals = workloads.u32_uniform(n, 9), workloads.index_payload(n)
+    dk, dv = to_dev(keys), to_dev(vals)
+    ko, vo = poisoned_like(dk), poisoned_like(dv)
+    assert call_noalloc(lib, dk, dv, ko, vo, n) == rs.RS_OK  # the array's address is known
+    assert rs.noalloc_status() == rs.RS_OK
+    assert rs.noalloc_timeout_probe(2_000_000) == rs.RS_ERR_LOOKBACK_TIMEOUT
+    assert rs.noalloc_status() == rs.RS_ERR_LOOKBACK_TIMEOUT
+    # the next sort starts from a clear status and is right
+    ko, vo = poisoned_like(dk), poisoned_like(dv)
+    assert call_noalloc(lib, dk, dv, ko, vo, n) == rs.RS_OK
+    assert rs.noalloc_status() == rs.RS_OK
+    ek, ev = oracle.sort(keys, vals, 0, 32, 8)
+    assert np.array_equal(to_host(ko, np.uint32), ek)
+    assert np.array_equal(to_host(vo, np.uint32), ev)
