@@ -14,10 +14,15 @@
 // and descending order complements T (pos and neg complemented), so that
 // equal patterns still keep input order.  fp16 and bf16 share the float
 // layout (FlagTree PR #1084 folds the descending flag into the key
-// conversion of every load).  T is applied on the fly at every digit
-// extraction and never stored: the stored bits are carried unchanged, so no
-// inverse is needed on the way out.  encode() gives T(k) whole, for callers
-// that take several digits of one key (the upfront histogram).
+// conversion of every load).  encode() gives T(k) whole.  The scatter
+// passes of signed, float or descending 32/64-bit keys apply T once, when
+// the first pass run loads a key, carry T(k) through the ping-pong buffers
+// and invert it when the last pass run writes the key out ("100 Days of
+// GPU", day 35: a bijection on the way in, its inverse on the way out):
+// `Stored` names the encoding whose digits those passes take from T(k), and
+// decode() is the inverse.  Every other key type is carried as stored
+// (`Stored` is the type itself) and T is applied at each digit extraction.
+// The upfront histogram always reads the caller's keys and applies T.
 #pragma once
 #include <cstdint>
 
@@ -33,6 +38,7 @@ namespace lsdrs {
 // Unsigned 32-bit keys in ascending order: T is the identity.
 struct KeyU32 {
   using T = uint32_t;
+  using Stored = KeyU32;
   static constexpr int kBits = 32;
   __device__ __forceinline__ static uint32_t encode(T k, const KeyXform&) { return k; }
   __device__ __forceinline__ static uint32_t digit(T k, int shift, uint32_t mask,
@@ -48,10 +54,18 @@ struct KeyU32 {
 // Any other 32-bit key: signed or float, or descending.
 struct KeyX32 {
   using T = uint32_t;
+  using Stored = KeyU32;  // the scatter passes carry T(k)
   static constexpr int kBits = 32;
   __device__ __forceinline__ static uint32_t encode(T k, const KeyXform& x) {
     return k ^ (static_cast<int32_t>(k) < 0 ? static_cast<uint32_t>(x.neg)
                                             : static_cast<uint32_t>(x.pos));
+  }
+  // The inverse of T: pos and neg have the same top bit for every key type
+  // and direction, so the top bit of T(k) ^ pos is the top bit of k.
+  __device__ __forceinline__ static uint32_t decode(uint32_t t, const KeyXform& x) {
+    return t ^ (static_cast<int32_t>(t ^ static_cast<uint32_t>(x.pos)) < 0
+                    ? static_cast<uint32_t>(x.neg)
+                    : static_cast<uint32_t>(x.pos));
   }
   __device__ __forceinline__ static uint32_t digit(T k, int shift, uint32_t mask,
                                                    const KeyXform& x) {
@@ -67,6 +81,7 @@ struct KeyX32 {
 
 struct KeyU64 {
   using T = uint64_t;
+  using Stored = KeyU64;
   static constexpr int kBits = 64;
   __device__ __forceinline__ static uint64_t encode(T k, const KeyXform&) { return k; }
   __device__ __forceinline__ static uint32_t digit(T k, int shift, uint32_t mask,
@@ -81,9 +96,14 @@ struct KeyU64 {
 
 struct KeyX64 {
   using T = uint64_t;
+  using Stored = KeyU64;  // the scatter passes carry T(k)
   static constexpr int kBits = 64;
   __device__ __forceinline__ static uint64_t encode(T k, const KeyXform& x) {
     return k ^ (static_cast<int64_t>(k) < 0 ? x.neg : x.pos);
+  }
+  // The inverse of T (see KeyX32::decode).
+  __device__ __forceinline__ static uint64_t decode(uint64_t t, const KeyXform& x) {
+    return t ^ (static_cast<int64_t>(t ^ x.pos) < 0 ? x.neg : x.pos);
   }
   __device__ __forceinline__ static uint32_t digit(T k, int shift, uint32_t mask,
                                                    const KeyXform& x) {
@@ -100,6 +120,7 @@ struct KeyX64 {
 // 16-bit float keys (fp16 / bf16 bit patterns).
 struct KeyF16Bits {
   using T = uint16_t;
+  using Stored = KeyF16Bits;
   static constexpr int kBits = 16;
   // T(k) in the low 16 bits (the bits above are not part of the key)
   __device__ __forceinline__ static uint32_t encode(T k, const KeyXform& x) {
@@ -127,6 +148,7 @@ struct KeyF16Bits {
 // writes the value out (bits): a digit is then one byte permute.
 struct KeyF16Packed {
   using T = uint32_t;
+  using Stored = KeyF16Packed;
   static constexpr int kBits = 16;
   __device__ __forceinline__ static uint32_t pack(uint16_t bits, uint32_t col,
                                                   const KeyXform& x) {

@@ -310,6 +310,11 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   constexpr int WKEYS = kWarp * ITEMS;
   constexpr bool kVals = VK == kValU32 || VK == kValIdx;  // a payload array travels
   constexpr bool kPack = VK == kValPack16;                // column index inside the key word
+  // Keys whose transform is applied once (signed, float, descending): the
+  // registers and ping-pong buffers hold T(k), whose digits are DK's.
+  using DK = typename KeyOp::Stored;
+  constexpr bool kEnc = !std::is_same<DK, KeyOp>::value;
+  const PassBufs<DYN> pass{DYN ? s.code : a.code, a};
 
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -327,7 +332,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
     // The tile's keys were bulk-copied into the stage buffer (16-byte
     // transfers, waited for by the caller); each thread reads its items
     // warp-striped from there.
-    if (kPack && PassBufs<DYN>{DYN ? s.code : a.code, a}.first()) {
+    if (kPack && pass.first()) {
       const uint16_t* st16 = reinterpret_cast<const uint16_t*>(io.stage_keys);
 #pragma unroll
       for (int i = 0; i < ITEMS; ++i) {
@@ -338,7 +343,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
 #pragma unroll
       for (int i = 0; i < ITEMS; ++i) keys[i] = io.stage_keys[wpos + i * kWarp];
     }
-  } else if (kPack && PassBufs<DYN>{DYN ? s.code : a.code, a}.first()) {
+  } else if (kPack && pass.first()) {
     // the row's 16-bit keys, transformed and packed with their columns
     const uint16_t* src16 = reinterpret_cast<const uint16_t*>(io.key_src);
 #pragma unroll
@@ -358,6 +363,12 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
                     ? io.key_src[wpos + i * kWarp]
                     : T(0);
   }
+  if constexpr (kEnc) {
+    if (pass.first()) {
+#pragma unroll
+      for (int i = 0; i < ITEMS; ++i) keys[i] = static_cast<T>(KeyOp::encode(keys[i], a.xf));
+    }
+  }
 
   // ---- 3. rank within the warp ------------------------------------------
   // The rank of item i among the warp's keys of its digit (below
@@ -370,7 +381,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   const uint32_t lt = lanemask_lt();
 #pragma unroll
   for (int i = 0; i < ITEMS; ++i) {
-    uint32_t d = pass_digit<KeyOp, BYTE>(keys[i], a);
+    uint32_t d = pass_digit<DK, BYTE>(keys[i], a);
     if (!FULL && wpos + i * kWarp >= valid) d = R - 1;
     const uint32_t peers = digit_peers<BITS>(d);
     // Every peer lane reads the warp's count of its digit (one word per
@@ -438,7 +449,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   auto half = [](uint32_t w, int i) -> uint32_t { return (i & 1) ? (w >> 16) : (w & 0xFFFFu); };
   auto item_digit = [&](int i) -> uint32_t {
     if (!FULL && wpos + i * kWarp >= valid) return R - 1;
-    return pass_digit<KeyOp, BYTE>(keys[i], a);
+    return pass_digit<DK, BYTE>(keys[i], a);
   };
   // Two items at a time: their warp offsets are packed like their ranks,
   // so one add gives both staging slots (each below TILE < 2^16, so the low
@@ -514,6 +525,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
   uint32_t* vout32 = static_cast<uint32_t*>(pb.template vals_out<VK>()) + row_base;
   int64_t* vout64 = static_cast<int64_t*>(pb.template vals_out<VK>()) + row_base;
   const bool wide = VK == kValIdx && pb.last();
+  const bool last_run = pb.last();  // (kEnc) write T^-1 of the carried keys
   if (kPack && pb.last()) {
     // the packed words leave as the row's values and their int64 columns
     uint16_t* v16 = static_cast<uint16_t*>(pb.keys_out()) + row_base;
@@ -522,7 +534,7 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
       const int j = i * THREADS + tid;
       if (FULL || j < valid) {
         const T k = io.stage_keys[j];
-        const uint32_t d = pass_digit<KeyOp, BYTE>(k, a);
+        const uint32_t d = pass_digit<DK, BYTE>(k, a);
         if (!in_bounds(d < R, a.error, 6)) continue;
         const uint32_t g = s.g_off[d] + static_cast<uint32_t>(j);
         if (!in_bounds(g < a.cols, a.error, 7)) continue;
@@ -539,11 +551,14 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
       const T k = io.stage_keys[j];
       uint32_t v = 0;
       if constexpr (kVals) v = io.vals[j];
-      const uint32_t d = pass_digit<KeyOp, BYTE>(k, a);
+      const uint32_t d = pass_digit<DK, BYTE>(k, a);
       if (!in_bounds(d < R, a.error, 6)) continue;
       const uint32_t g = s.g_off[d] + static_cast<uint32_t>(j);
       if (!in_bounds(g < a.cols, a.error, 7)) continue;
-      kout[g] = k;
+      if constexpr (kEnc)
+        kout[g] = last_run ? static_cast<T>(KeyOp::decode(k, a.xf)) : k;
+      else
+        kout[g] = k;
       if constexpr (kVals) {
         if (wide)
           vout64[g] = static_cast<int64_t>(static_cast<int32_t>(v));
