@@ -41,7 +41,7 @@ struct SweepShape {
 // are the fastest measured on GB300 for 2^28-key sorts.
 #ifndef LSDRS_U32K_T
 #define LSDRS_U32K_T 256
-#define LSDRS_U32K_I 28
+#define LSDRS_U32K_I 30
 #define LSDRS_U32K_B 4
 #endif
 #ifndef LSDRS_U32K_W
