@@ -117,6 +117,37 @@ def test_typed_skips_on_transformed_digits(rs, in_place):
         assert np.array_equal(vo, ev) and run == 3
 
 
+# Signed, float and descending keys carry T(k) between the first and the
+# last pass run: one pass run (first and last at once), none (the input is
+# copied), an even and an odd number in place, for 32- and 64-bit keys.
+TYPED_CASES = {
+    "i32_one_byte": (lambda n: (workloads.u32_uniform(n, 11) & np.uint32(0xFF)).astype(np.int32),
+                     "i32", 1),
+    "i32_all_equal": (lambda n: np.full(n, -12345, np.int32), "i32", 0),
+    "i64_two_bytes": (lambda n: (workloads.u64_uniform(n, 12) & np.uint64(0xFFFF)).astype(np.int64),
+                      "i64", 2),
+    "f64_seven_bytes": (lambda n: 1.0 + (workloads.u64_uniform(n, 13) >> np.uint64(12)).astype(
+        np.float64) / 2.0**52, "f64", 7),
+}
+
+
+@pytest.mark.parametrize("case", sorted(TYPED_CASES))
+@pytest.mark.parametrize("in_place", [False, True])
+@pytest.mark.parametrize("descending", [False, True])
+def test_typed_passes_run_carry_the_transform(rs, case, in_place, descending):
+    gen, key_type, want = TYPED_CASES[case]
+    n = 40_001
+    x = gen(n)
+    vals = workloads.index_payload(n)
+    ek, ev = oracle.sort_typed(x, key_type, vals, descending)
+    end = 8 * x.dtype.itemsize
+    ko, vo, run = sort_pairs(rs, x, vals, 0, end, 8, in_place, key_type=key_type,
+                             descending=descending)
+    u = np.uint32 if x.dtype.itemsize == 4 else np.uint64
+    assert np.array_equal(ko.view(u), ek.view(u))
+    assert np.array_equal(vo, ev) and run == want
+
+
 def _rows_sort(rs, x, descending, in_place=False):
     d = torch.from_numpy(x.view(np.int16)).cuda().view(torch.float16)
     temp = torch.empty(rs.segmented_temp_bytes(*x.shape), dtype=torch.uint8, device="cuda")
