@@ -613,8 +613,8 @@ def main():
     ap.add_argument("--no-configs", action="store_true")
     ap.add_argument("--no-cpu-configs", action="store_true")
     ap.add_argument("--details", default=None,
-                    help="file for the bulky tables (default: gpurun_out/bench_details.json "
-                         "when that folder exists, else bench_details.json)")
+                    help="file for the bulky tables (default: bench_details.json at the "
+                         "repository root)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -920,7 +920,7 @@ def main():
                 "distributions": dists, "configs": cfg_tab,
                 "small_sorts_us_stream_graph": small, "keys_only_configs": keys_cfg,
                 "row_sorts_ms_lookback_precomputed_torch": rows_tab}
-        path = args.details or os.path.join(ROOT, "gpurun_out", "bench_details.json")
+        path = os.path.abspath(args.details or os.path.join(ROOT, "bench_details.json"))
         try:
             os.makedirs(os.path.dirname(path), exist_ok=True)
             with open(path, "w") as f:
