@@ -141,7 +141,7 @@ rs_status make_plan(KeyKind key, ValKind val, int64_t rows, int64_t cols, int be
   p.radix = 1 << bits;
   const int last_w = end_bit - (begin_bit + (p.passes - 1) * bits);
   p.last_mask = (1u << last_w) - 1u;
-  p.tile = sweep_shape(key, val).tile();
+  p.tile = sweep_shape(key, val, rows, cols).tile();
   p.tiles_per_row = cdiv(cols, p.tile);
   p.tiles = rows * p.tiles_per_row;
   if (p.tiles > static_cast<int64_t>(kTileMask)) return RS_ERR_INVALID;  // tile ids: 24 bits

@@ -93,8 +93,23 @@ constexpr SweepShape kShapeU64Keys{LSDRS_U64K_T, LSDRS_U64K_I, LSDRS_U64K_B, LSD
 constexpr SweepShape kShapeU64Pairs{LSDRS_U64P_T, LSDRS_U64P_I, LSDRS_U64P_B, LSDRS_U64P_W};
 constexpr SweepShape kShapeF16Idx{LSDRS_F16_T, LSDRS_F16_I, LSDRS_F16_B, LSDRS_F16_W};
 constexpr SweepShape kShapeF16Packed{LSDRS_F16P_T, LSDRS_F16P_I, LSDRS_F16P_B, LSDRS_F16P_W};
-constexpr SweepShape sweep_shape(KeyKind k, ValKind v) {
-  return (k == kKeyU32 || k == kKeyX32) ? (v == kValNone ? kShapeU32Keys : kShapeU32Pairs)
+// Flat u32 sorts of at most kMidMaxKeys keys take smaller tiles: each pass
+// is a fraction of one wave of CTAs, so a tile's serial chain (load, rank,
+// look-back, write) sets the pass time, and a shorter tile shortens it
+// (measured: 2^16 keys 34.2 -> 32.1 us, 2^16 pairs 38.0 -> 35.0 us per
+// sort launched on a stream); from 2^20 keys on the larger tiles are faster.
+#ifndef LSDRS_MID_MAX_KEYS
+#define LSDRS_MID_MAX_KEYS (1 << 18)
+#endif
+constexpr int64_t kMidMaxKeys = LSDRS_MID_MAX_KEYS;
+constexpr SweepShape kShapeU32KeysMid{256, 14, 4, 8};
+constexpr SweepShape kShapeU32PairsMid{256, 12, 4, 4};
+constexpr bool mid_tiles(KeyKind k, ValKind v, int64_t rows, int64_t cols) {
+  return k == kKeyU32 && v != kValIdx && rows == 1 && cols <= kMidMaxKeys;
+}
+constexpr SweepShape sweep_shape(KeyKind k, ValKind v, int64_t rows, int64_t cols) {
+  return mid_tiles(k, v, rows, cols)     ? (v == kValNone ? kShapeU32KeysMid : kShapeU32PairsMid)
+       : (k == kKeyU32 || k == kKeyX32) ? (v == kValNone ? kShapeU32Keys : kShapeU32Pairs)
        : (k == kKeyU64 || k == kKeyX64) ? (v == kValNone ? kShapeU64Keys : kShapeU64Pairs)
        : v == kValPack16                ? kShapeF16Packed
                                         : kShapeF16Idx;
@@ -239,6 +254,8 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
 // kernels launched (0 or 1).
 cudaError_t launch_sweep_u32(ValKind v, int bits, const SweepArgs& a, int* launched,
                              cudaStream_t s);
+cudaError_t launch_sweep_u32_mid(ValKind v, int bits, const SweepArgs& a, int* launched,
+                                 cudaStream_t s);
 cudaError_t launch_sweep_u64(ValKind v, int bits, const SweepArgs& a, int* launched,
                              cudaStream_t s);
 cudaError_t launch_sweep_x32(ValKind v, int bits, const SweepArgs& a, int* launched,

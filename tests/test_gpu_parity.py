@@ -13,7 +13,9 @@ pytestmark = pytest.mark.gpu
 
 # tile sizes of the sweep kernels (keys per CTA), so that ragged cases
 # straddle tile boundaries
-TILE_U32_KEYS, TILE_U32_PAIRS, TILE_U64, TILE_U64_PAIRS, TILE_F16 = 7168, 5888, 4096, 4608, 6144
+TILE_U32_KEYS, TILE_U32_PAIRS, TILE_U64, TILE_U64_PAIRS, TILE_F16 = 7680, 5888, 4096, 4608, 6144
+# flat u32 sorts of at most MID_MAX keys use the smaller mid-size tiles
+MID_KEYS, MID_PAIRS, MID_MAX = 3584, 3072, 1 << 18
 
 
 def run_keys(rs, keys, begin=0, end=None, bits=8, **opts):
@@ -93,9 +95,8 @@ def test_u64_pairs_and_keys(rs, dist, begin, end):
 # ---------------------------------------------------- ragged and degenerate
 
 RAGGED = [1, 2, 31, 32, 33, 1000, TILE_U64 - 1, TILE_U64, TILE_U64 + 1, TILE_U64_PAIRS - 1,
-          TILE_U64_PAIRS + 1, TILE_U32_PAIRS - 1,
-          TILE_U32_PAIRS + 1, TILE_U32_KEYS - 1, TILE_U32_KEYS, TILE_U32_KEYS + 1,
-          3 * TILE_U32_KEYS + 17, 100_003]
+          TILE_U64_PAIRS + 1, MID_PAIRS - 1, MID_PAIRS + 1, MID_KEYS - 1, MID_KEYS,
+          MID_KEYS + 1, 3 * MID_KEYS + 17, 100_003]
 
 
 @pytest.mark.parametrize("n", RAGGED)
@@ -119,6 +120,20 @@ def test_ragged_sizes(rs, n, small_sort):
     k64o, v64o = run_pairs(rs, k64, vals, 0, 64, 8, **o)
     e64, ev64 = oracle.sort(k64, vals, 0, 64, 8)
     assert_pairs(k64o, v64o, e64, ev64)
+
+
+@pytest.mark.parametrize("n", [MID_MAX, MID_MAX + 1, 36 * TILE_U32_KEYS, 36 * TILE_U32_KEYS + 1,
+                               45 * TILE_U32_PAIRS - 1, 45 * TILE_U32_PAIRS + 1])
+def test_tile_shapes_either_side_of_mid_size(rs, n):
+    # up to MID_MAX keys the mid-size tiles, above it the large ones, with
+    # full and partial last tiles of each
+    keys = workloads.u32_uniform(n, 31)
+    keys[::4] = keys[1]
+    vals = workloads.index_payload(n)
+    ko, vo = run_pairs(rs, keys, vals, 0, 32, 8)
+    ek, ev = oracle.sort(keys, vals, 0, 32, 8)
+    assert_pairs(ko, vo, ek, ev)
+    assert np.array_equal(run_keys(rs, keys, 0, 32, 8), ek)
 
 
 @pytest.mark.parametrize("bits", [1, 2, 3, 4, 5, 6, 7, 8])
