@@ -57,7 +57,7 @@ struct SweepShape {
 #endif
 #ifndef LSDRS_U64K_T
 #define LSDRS_U64K_T 256
-#define LSDRS_U64K_I 16
+#define LSDRS_U64K_I 22
 #define LSDRS_U64K_B 3
 #endif
 #ifndef LSDRS_U64K_W

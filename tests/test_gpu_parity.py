@@ -13,7 +13,7 @@ pytestmark = pytest.mark.gpu
 
 # tile sizes of the sweep kernels (keys per CTA), so that ragged cases
 # straddle tile boundaries
-TILE_U32_KEYS, TILE_U32_PAIRS, TILE_U64, TILE_U64_PAIRS, TILE_F16 = 7680, 5888, 4096, 4608, 6144
+TILE_U32_KEYS, TILE_U32_PAIRS, TILE_U64, TILE_U64_PAIRS, TILE_F16 = 7680, 5888, 5632, 4608, 6144
 # flat u32 sorts of at most MID_MAX keys use the smaller mid-size tiles
 MID_KEYS, MID_PAIRS, MID_MAX = 3584, 3072, 1 << 18
 

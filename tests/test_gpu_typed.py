@@ -12,7 +12,7 @@ from tests.gpu_util import poisoned_like, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
-TILE_32_KEYS, TILE_32_PAIRS, TILE_64_KEYS, TILE_64_PAIRS = 7680, 5888, 4096, 4608
+TILE_32_KEYS, TILE_32_PAIRS, TILE_64_KEYS, TILE_64_PAIRS = 7680, 5888, 5632, 4608
 SIZES = [1, 2, 33, 1000, TILE_32_PAIRS - 1, TILE_32_PAIRS + 1, TILE_32_KEYS + 1,
          TILE_64_PAIRS + 1, 3 * TILE_32_KEYS + 17, 100_003]
 TYPES = {"i32": np.int32, "f32": np.float32, "i64": np.int64, "f64": np.float64,
