@@ -332,9 +332,15 @@ rs_status run_sort(Plan p, const void* keys_in, void* keys_out, const void* vals
   // stages one word per key; their tile is the packed kernel's.
   const bool packed = p.val == kValIdx && !precomputed && !dynamic && p.cols <= kPackMaxCols;
   if (packed) {
+    // The scratch is planned for the unpacked tile; the packed tile is at
+    // least as large (checked at compile time), so its look-back words fit.
+    static_assert(kShapeF16Packed.tile() >= kShapeF16Idx.tile(),
+                  "packed row tiles must not outnumber the planned tiles");
+    const int64_t planned = p.tiles;
     p.tile = kShapeF16Packed.tile();
     p.tiles_per_row = cdiv(p.cols, p.tile);
-    p.tiles = p.rows * p.tiles_per_row;  // fewer than planned: the look-back arrays fit
+    p.tiles = p.rows * p.tiles_per_row;
+    if (p.tiles > planned) return RS_ERR_INVALID;
   }
   configure(&p);
   rs_status st = run_front(p, keys_in, xf, temp, nullptr, nullptr, in_place, dynamic, s);
