@@ -372,6 +372,13 @@ rs_status run_sort(Plan p, const void* keys_in, void* keys_out, const void* vals
   a.bases_row_stride = static_cast<int64_t>(p.passes) * p.radix;
   a.error = header + kHdrError;
   a.timeout_ns = opt.timeout_ns;
+  // flat sorts: prefetch, per tile, the keys of the tile taken about one
+  // resident grid (LSDRS_PREFETCH_AHEAD_PCT percent of it) later
+  a.prefetch_tiles =
+      p.rows == 1 ? static_cast<uint32_t>(device_sm_count() *
+                                          sweep_shape(p.key, p.val, p.rows, p.cols).min_blocks *
+                                          LSDRS_PREFETCH_AHEAD_PCT / 100)
+                  : 0u;
   a.dynamic = dynamic ? 1 : 0;
   uint32_t prev = kBufIn;
   for (int q = 0; q < p.passes; ++q) {

@@ -127,6 +127,13 @@ __device__ __forceinline__ T ld_stream(const T* p) {
   return __ldcs(p);
 }
 
+// A hint that the 128-byte line at global address p will be read soon:
+// fetch it into L2 (no fault, no result).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile(
+      "{\n\t.reg .u64 g;\n\tcvta.to.global.u64 g, %0;\n\tprefetch.global.L2 [g];\n\t}" ::"l"(p));
+}
+
 // ---- mbarrier + 1-D bulk copy (TMA) helpers -------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

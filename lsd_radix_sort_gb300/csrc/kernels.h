@@ -244,6 +244,11 @@ struct SweepArgs {
   const uint32_t* offsets; // [rows * tiles_per_row][radix] precomputed output offsets, or null
   uint32_t* error;
   uint64_t timeout_ns;
+  uint32_t prefetch_tiles;  // tiles ahead whose keys a tile prefetches into L2
+                            // (about the CTAs resident at once; 0: none)
+#ifndef LSDRS_PREFETCH_AHEAD_PCT
+#define LSDRS_PREFETCH_AHEAD_PCT 35
+#endif
 };
 
 cudaError_t launch_hist(KeyKind k, int bits, const HistArgs& a, int grid, cudaStream_t s);
