@@ -612,6 +612,8 @@ def main():
     ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--no-configs", action="store_true")
     ap.add_argument("--no-cpu-configs", action="store_true")
+    ap.add_argument("--e2e-sets", type=int, default=2,
+                    help="device buffer sets the pipelined end-to-end schedule rotates through")
     ap.add_argument("--details", default=None,
                     help="file for the bulky tables (default: bench_details.json at the "
                          "repository root)")
@@ -724,14 +726,17 @@ def main():
         # Every step copies its keys and payloads from pinned host memory,
         # sorts them through the public API, and copies the sorted keys and
         # payloads back.  Serial: one step after the other on one stream.
-        # Pipelined (reported as `e2e`): two device buffer sets; step i's
+        # Pipelined (reported as `e2e`): device buffer sets (two by default); step i's
         # upload, sort and readback are ordered by events, so step i's
         # readback overlaps step i+1's upload and sort (the link carries both
         # directions at once); each step still moves all of its own bytes.
+        # An upload into a set waits only for the sort that last read that
+        # set's inputs; the sort waits for its upload and for the readback of
+        # the set's previous outputs, which it overwrites.
         hk = torch.from_numpy(keys.view(np.int32)).pin_memory()
         hv = torch.from_numpy(vals.view(np.int32)).pin_memory()
         sets = []
-        nsets = 2
+        nsets = args.e2e_sets
         for _ in range(nsets):
             sets.append({"dk": torch.empty_like(dk), "dv": torch.empty_like(dv),
                          "ko": torch.empty_like(dk), "vo": torch.empty_like(dv),
@@ -749,22 +754,26 @@ def main():
             b["hko"].copy_(b["ko"], non_blocking=True)
             b["hvo"].copy_(b["vo"], non_blocking=True)
 
-        freed = [None] * nsets
+        freed = [None] * nsets     # the set's last readback is done
+        consumed = [None] * nsets  # the set's last sort is done (its inputs are free)
 
         def pipelined_step(i):
             b = sets[i % nsets]
             with torch.cuda.stream(up):
-                if freed[i % nsets] is not None:
-                    up.wait_event(freed[i % nsets])  # the set's last readback is done
+                if consumed[i % nsets] is not None:
+                    up.wait_event(consumed[i % nsets])
                 b["dk"].copy_(hk, non_blocking=True)
                 b["dv"].copy_(hv, non_blocking=True)
                 loaded = torch.cuda.Event()
                 loaded.record(up)
             comp.wait_event(loaded)
+            if freed[i % nsets] is not None:
+                comp.wait_event(freed[i % nsets])
             rs.radix_sort_pairs(b["dk"], b["dv"], b["ko"], b["vo"], 0, 32, DIGIT_BITS,
                                 temp=b["temp"], stream=comp)
             sorted_ev = torch.cuda.Event()
             sorted_ev.record(comp)
+            consumed[i % nsets] = sorted_ev
             with torch.cuda.stream(down):
                 down.wait_event(sorted_ev)
                 b["hko"].copy_(b["ko"], non_blocking=True)
