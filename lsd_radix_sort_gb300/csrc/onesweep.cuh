@@ -118,6 +118,24 @@ constexpr int kPhaseWord = 104;
   } while (0)
 #endif
 
+// A store of the pass's output: evict-first (streaming) when
+// LSDRS_STREAM_STORES, so that the output, which the next pass reads only
+// after the whole pass, does not push the prefetched keys out of L2.
+#ifndef LSDRS_STREAM_STORES
+#define LSDRS_STREAM_STORES 1
+#endif
+template <class V>
+__device__ __forceinline__ void out_store(V* p, V v) {
+  if constexpr (LSDRS_STREAM_STORES && (sizeof(V) == 4 || sizeof(V) == 8)) {
+    if constexpr (sizeof(V) == 4)
+      __stcs(reinterpret_cast<unsigned int*>(p), static_cast<unsigned int>(v));
+    else
+      __stcs(reinterpret_cast<unsigned long long*>(p), static_cast<unsigned long long>(v));
+  } else {
+    *p = v;
+  }
+}
+
 // This pass's digit of key k: one byte permute when the digit is a whole
 // byte of the transformed key (BYTE), else shift and mask.
 template <class KeyOp, bool BYTE>
@@ -567,15 +585,14 @@ __device__ __forceinline__ void sweep_tile(const SweepArgs& a,
       if (!in_bounds(d < R, a.error, 6)) continue;
       const uint32_t g = s.g_off[d] + static_cast<uint32_t>(j);
       if (!in_bounds(g < a.cols, a.error, 7)) continue;
-      if constexpr (kEnc)
-        kout[g] = last_run ? static_cast<T>(KeyOp::decode(k, a.xf)) : k;
-      else
-        kout[g] = k;
+      T kw = k;
+      if constexpr (kEnc) kw = last_run ? static_cast<T>(KeyOp::decode(k, a.xf)) : k;
+      out_store(kout + g, kw);
       if constexpr (kVals) {
         if (wide)
-          vout64[g] = static_cast<int64_t>(static_cast<int32_t>(v));
+          out_store(vout64 + g, static_cast<int64_t>(static_cast<int32_t>(v)));
         else
-          vout32[g] = v;
+          out_store(vout32 + g, v);
       }
     }
   }
