@@ -92,6 +92,36 @@ struct KeyCounter {
       mask[p] = p == np - 1 ? lm : static_cast<uint32_t>(R - 1);
     }
   }
+  // The keys of one 16-byte load.  For 16-bit float keys with byte digits
+  // (the row-wise sorts) two keys are transformed at once per 32-bit word:
+  // T(u) = u ^ pos ^ (sign(u) ? pos ^ neg : 0) in each half, the sign bits
+  // taken to bits 0 and 16 and multiplied by pos ^ neg (below 2^16, so the
+  // halves never carry into each other).
+  __device__ __forceinline__ void add_vec(const uint4& b) const {
+    if constexpr (BYTES && std::is_same<KeyOp, KeyF16Bits>::value) {
+      const uint32_t pos = static_cast<uint32_t>(xf.pos) & 0xFFFFu;
+      const uint32_t diff = (static_cast<uint32_t>(xf.pos) ^ static_cast<uint32_t>(xf.neg)) & 0xFFFFu;
+      const uint32_t pos2 = pos * 0x10001u;
+      const uint32_t w4[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t w = w4[q];
+        const uint32_t t = w ^ pos2 ^ (((w >> 15) & 0x00010001u) * diff);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {      // key h of the word
+#pragma unroll
+          for (int p = 0; p < 2; ++p) {    // its two byte digits
+            const uint32_t d = __byte_perm(t, 0u, 0x4440u + 2 * h + p);
+            if (in_bounds(d < R, hdr, 10)) atomicAdd(col + (p * R + d) * C, 1u);
+          }
+        }
+      }
+    } else {
+      const typename KeyOp::T* ks = reinterpret_cast<const typename KeyOp::T*>(&b);
+#pragma unroll
+      for (int e = 0; e < 16 / static_cast<int>(sizeof(typename KeyOp::T)); ++e) add(ks[e]);
+    }
+  }
   __device__ __forceinline__ void add(typename KeyOp::T k) const {
     if constexpr (BYTES) {
       const auto t = KeyOp::encode(k, xf);
@@ -150,18 +180,11 @@ __device__ __forceinline__ void count_range(const typename KeyOp::T* base, int64
                    ? __ldcs(vp + v + u * Cfg::kThreads)
                    : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const T* ks = reinterpret_cast<const T*>(&buf[u]);
-#pragma unroll
-      for (int e = 0; e < V; ++e) c.add(ks[e]);
-    }
+    for (int u = 0; u < U; ++u) c.add_vec(buf[u]);
   }
   for (; v < nvec; v += Cfg::kThreads) {
     if (!in_bounds(body_begin + (v + 1) * V <= cols, c.hdr, 16)) continue;
-    uint4 b = __ldcs(vp + v);
-    const T* ks = reinterpret_cast<const T*>(&b);
-#pragma unroll
-    for (int e = 0; e < V; ++e) c.add(ks[e]);
+    c.add_vec(__ldcs(vp + v));
   }
 }
 
